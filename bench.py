@@ -1,0 +1,525 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused reduce + residual add + RMSNorm (+ FP8) epilogue.
+
+Headline workload (one "step"): the decode configuration R=8 partials, H=7168,
+one fused call at each of T = 8, 16, 32 and 64 tokens (no quant).  The metric
+is effective GB/s -- algorithmic HBM bytes of the step over its device time --
+next to its fraction of the measured HBM peak, plus microseconds per call at
+each decode T.  Each step reads a different one of several rotating input
+sets whose total size exceeds twice the L2, so no step hits inputs the previous
+one left in L2.  Steps run as CUDA-graph replays (one graph per input set, four
+launches each), as a decode engine records them.
+
+Besides the JSON contract keys, the line carries:
+  decode_us_per_call  per T: graph replay and raw (Python-launched) calls
+  large_T             the >= 1024-token workloads: the message sweep at
+                      16/32/64 MB per partial and the 8192-token prefill chunk
+                      with per-group FP8 quant (both output variants), each with
+                      effective GB/s and fraction of HBM peak
+  sweep               all 12 message sizes, 32 KB .. 64 MB per partial
+  roofline            the dominant kernel of the step (the T=64 call)
+  cpu_baseline        the CPU oracle on this host's cores, on a bounded sample
+  e2e                 the step through the public API with pinned host buffers,
+                      host->device copies of the inputs and device->host reads
+                      of the outputs inside the timed region
+
+``--impl reference`` times the CPU oracle (the reference arm) on the same
+workload and metric instead.  Under torchrun every rank runs its own replica of
+the workload on its own GPU (replicas only: the op has no cross-GPU exchange);
+the timed region is bracketed by a barrier and the max time over ranks counts.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from reduce_residual_rmsnorm_fp32_gb300 import synthetic as syn  # noqa: E402
+
+R_DEC = 8
+H = syn.H_DEEPSEEK
+DECODE_T = syn.DECODE_TOKENS
+EPS = 1e-6
+METRIC = "fused reduce+RMSNorm(+FP8) effective GB/s, % of HBM peak; µs/call at decode T"
+WORKLOAD = "decode R=8 H=7168 T={8,16,32,64} bf16, residual_out + RMSNorm y, no quant"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def step_bytes():
+    return sum(syn.algorithmic_bytes(R_DEC, T, H, "norm") for T in DECODE_T)
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------ dist setup --
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ GPU timing --
+
+def l2_bytes():
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 129 * 2 ** 20
+
+
+def sets_to_beat_l2(footprint: int) -> int:
+    """Rotating input sets needed so that the data touched between two uses of
+    one set exceeds 2.2x the L2 (each set is evicted before it is reused)."""
+    return max(1, math.ceil(2.2 * l2_bytes() / max(footprint, 1)))
+
+
+class DecodeSet:
+    """Device buffers of one decode input set: the four T values."""
+
+    def __init__(self, seed: int, gamma):
+        self.bufs = {}
+        for i, T in enumerate(DECODE_T):
+            p, r, _ = syn.make_inputs_device(R_DEC, T, H, seed=seed * 100 + i, partial_std=0.5)
+            ro = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+            y = torch.empty_like(ro)
+            self.bufs[T] = (p, r, ro, y)
+        self.gamma = gamma
+
+    def call(self, frn, T):
+        p, r, ro, y = self.bufs[T]
+        frn.fused_reduce_rmsnorm(p, r, self.gamma, EPS, residual_out=ro, y=y)
+
+    def step(self, frn):
+        for T in DECODE_T:
+            self.call(frn, T)
+
+
+def capture(fn, warm: int = 1):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warm):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def time_graph(g, calls_per_replay: int, min_seconds: float = 0.05, max_reps: int = 20000):
+    """Mean device time per call of a graph holding `calls_per_replay` calls."""
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    one = max(e0.elapsed_time(e1) / 1e3, 1e-7)
+    reps = int(min(max_reps, max(3, min_seconds / one)))
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (reps * calls_per_replay)
+
+
+def measure_decode_per_T(frn):
+    """µs per call at each decode T: graph replay over enough rotating sets to
+    defeat L2, and raw calls launched one by one from Python."""
+    out = {}
+    gamma = syn.make_inputs_device(1, 1, H, seed=7)[2]
+    for T in DECODE_T:
+        fp = syn.algorithmic_bytes(R_DEC, T, H, "norm")
+        n = sets_to_beat_l2(fp)
+        sets = []
+        for k in range(n):
+            p, r, _ = syn.make_inputs_device(R_DEC, T, H, seed=1000 + k, partial_std=0.5)
+            sets.append((p, r, torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
+                         torch.empty((T, H), dtype=torch.bfloat16, device="cuda")))
+
+        def body():
+            for p, r, ro, y in sets:
+                frn.fused_reduce_rmsnorm(p, r, gamma, EPS, residual_out=ro, y=y)
+        g = capture(body)
+        t_graph = time_graph(g, n, min_seconds=0.1)
+        # raw launches
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(1, 2000 // n)
+        e0.record()
+        for _ in range(reps):
+            body()
+        e1.record()
+        torch.cuda.synchronize()
+        t_raw = e0.elapsed_time(e1) / 1e3 / (reps * n)
+        out[str(T)] = {"graph_us": round(t_graph * 1e6, 3), "raw_launch_us": round(t_raw * 1e6, 3),
+                       "bytes": fp, "graph_GBps": round(fp / t_graph / 1e9, 1), "input_sets": n}
+        del sets, g
+    return out
+
+
+def measure_rows(frn, R, T, mode, seed, hbm, outlier=False, partial_std=0.5, H=H):
+    """Effective GB/s of one call shape, cold L2 (rotating sets or inputs larger
+    than L2)."""
+    fp = syn.algorithmic_bytes(R, T, H, mode)
+    n = sets_to_beat_l2(fp)
+    sets = []
+    for k in range(n):
+        p, r, g = syn.make_inputs_device(R, T, H, seed=seed + k, partial_std=partial_std,
+                                         outlier_frac=0.01 if outlier else 0.0)
+        ro = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        y = torch.empty_like(ro) if mode in ("norm", "quant_b") else None
+        q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device="cuda") if mode != "norm" else None
+        s = torch.empty((T, H // 128), dtype=torch.float32, device="cuda") if mode != "norm" else None
+        sets.append((p, r, g, ro, y, q, s))
+
+    def body():
+        for p, r, g, ro, y, q, s in sets:
+            if mode == "norm":
+                frn.fused_reduce_rmsnorm(p, r, g, EPS, residual_out=ro, y=y)
+            else:
+                frn.fused_reduce_rmsnorm_quant_per_group(p, r, g, EPS, 128, mode == "quant_b", residual_out=ro,
+                                                         y=y, q=q, scales=s)
+    gr = capture(body)
+    t = time_graph(gr, n, min_seconds=0.2)
+    del sets, gr
+    torch.cuda.empty_cache()
+    gbs = fp / t / 1e9
+    return {"R": R, "T": T, "H": H, "mode": mode, "us": round(t * 1e6, 2), "bytes": fp,
+            "GBps": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "input_sets": n}
+
+
+def measure_e2e(frn, steps: int):
+    """The decode step through the public API from pinned host buffers."""
+    host = {}
+    for i, T in enumerate(DECODE_T):
+        inp = syn.config_decode(T, seed=500 + i)
+        host[T] = (torch.from_numpy(inp.partials.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                   torch.from_numpy(inp.residual.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                   torch.empty((T, H), dtype=torch.bfloat16).pin_memory(),
+                   torch.empty((T, H), dtype=torch.bfloat16).pin_memory())
+    gamma_h = torch.from_numpy(syn.config_decode(8).gamma.view(np.int16)).view(torch.bfloat16).pin_memory()
+    dev = {T: (torch.empty_like(h[0], device="cuda"), torch.empty_like(h[1], device="cuda"),
+               torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((T, H), dtype=torch.bfloat16, device="cuda")) for T, h in host.items()}
+    gamma_d = torch.empty_like(gamma_h, device="cuda")
+    h2d = gamma_h.numel() * 2 + sum(h[0].numel() * 2 + h[1].numel() * 2 for h in host.values())
+    d2h = sum(2 * T * H * 2 for T in DECODE_T)
+
+    def one_step():
+        gamma_d.copy_(gamma_h, non_blocking=True)
+        for T in DECODE_T:
+            hp, hr, hro, hy = host[T]
+            dp, dr, dro, dy = dev[T]
+            dp.copy_(hp, non_blocking=True)
+            dr.copy_(hr, non_blocking=True)
+            frn.fused_reduce_rmsnorm(dp, dr, gamma_d, EPS, residual_out=dro, y=dy)
+            hro.copy_(dro, non_blocking=True)
+            hy.copy_(dy, non_blocking=True)
+
+    for _ in range(3):
+        one_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one_step()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    return t, h2d, d2h
+
+
+def cpu_baseline(seconds: float = 12.0):
+    """The CPU oracle, as it stands, on the host's cores: whole decode steps of
+    the workload (host-generated inputs) until about `seconds` have passed."""
+    import oracle
+    orc = oracle.Oracle()
+    cores = os.cpu_count() or 1
+    inps = [syn.config_decode(T, seed=900 + i) for i, T in enumerate(DECODE_T)]
+    nbytes, steps = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        for inp in inps:
+            orc.reduce_rmsnorm(inp.partials, inp.residual, inp.gamma, inp.eps, threads=cores)
+        steps += 1
+        nbytes += step_bytes()
+        el = time.perf_counter() - t0
+        if el >= seconds or steps >= 1000:
+            break
+    return {"value": round(nbytes / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} whole decode steps (T=8,16,32,64; R=8, H=7168), OpenMP rows over {cores} threads, "
+                      f"{el:.1f} s"}
+
+
+# ------------------------------------------------------------ reference --
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle on the same workload and metric.  Each step
+    processes a bounded sample of the decode step's 120 token rows (the first n
+    rows in T order), n sized so that warm-up plus timed steps take about 90 s."""
+    if rank != 0:
+        return
+    import oracle
+    orc = oracle.Oracle()
+    cores = os.cpu_count() or 1
+    inps = [syn.config_decode(T, seed=900 + i) for i, T in enumerate(DECODE_T)]
+    rows = []   # (partials [R,1,H], residual [1,H]) for every row of the step, in T order
+    for inp in inps:
+        for t in range(inp.T):
+            rows.append((inp.partials[:, t:t + 1].copy(), inp.residual[t:t + 1].copy()))
+    gamma = inps[0].gamma
+    t0 = time.perf_counter()
+    for p, r in rows[:2]:
+        orc.reduce_rmsnorm(p, r, gamma, EPS, threads=1)
+    per_row = (time.perf_counter() - t0) / 2
+    total_steps = args.steps + args.warmup
+    n = int(max(1, min(len(rows), 90.0 / max(total_steps, 1) / max(per_row, 1e-9))))
+    if n >= 16:
+        # whole blocks of rows, so that OpenMP can split them
+        sample = [syn.Inputs(np.concatenate([p for p, _ in rows[:n]], axis=1),
+                             np.concatenate([r for _, r in rows[:n]], axis=0), gamma, EPS)]
+    else:
+        sample = [syn.Inputs(p, r, gamma, EPS) for p, r in rows[:n]]
+    bytes_step = sum(syn.algorithmic_bytes(R_DEC, s.T, H, "norm") for s in sample)
+    thr = min(cores, n)
+
+    def step():
+        for s in sample:
+            orc.reduce_rmsnorm(s.partials, s.residual, s.gamma, EPS, threads=thr)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = bytes_step * args.steps / el / 1e9
+    desc = (f"each step: the first {n} of the decode step's {len(rows)} token rows (R=8, H=7168), "
+            f"OpenMP rows over {thr} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy, bf16 inputs)",
+        "config": {"workload": WORKLOAD, "R": R_DEC, "H": H, "T": list(DECODE_T), "reference": "CPU oracle (plain C)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["frn", "reference"], default="frn")
+    ap.add_argument("--no-extras", action="store_true", help="skip sweep / large-T / e2e / CPU legs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import reduce_residual_rmsnorm_fp32_gb300 as frn
+    frn.library()   # fails loudly if the CUDA library is missing
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm, peak_kind = peaks()
+
+    # ---- headline: decode steps over rotating input sets, as graph replays
+    per_set = sum(syn.algorithmic_bytes(R_DEC, T, H, "norm") for T in DECODE_T)
+    nsets = max(16, sets_to_beat_l2(per_set))
+    gamma = syn.make_inputs_device(1, 1, H, seed=3)[2]
+    sets = [DecodeSet(seed=rank * 10000 + k, gamma=gamma) for k in range(nsets)]
+    graphs = [capture(lambda s=s: s.step(frn)) for s in sets]
+    # clocks are sampled from here to the end of the timed region: a ~0.5 s
+    # stretch of the same steps first (part of the warm-up), then the timed steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.perf_counter() + 0.5
+    k = 0
+    while k < args.warmup or time.perf_counter() < t_end:
+        graphs[k % nsets].replay()
+        k += 1
+        if k % 256 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(args.steps):
+        graphs[k % nsets].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    bytes_per_step = step_bytes()
+    value = world * bytes_per_step * args.steps / elapsed / 1e9
+    del graphs, sets
+    torch.cuda.empty_cache()
+
+    extras = {}
+    roofline = None
+    if not args.no_extras:
+        dec = measure_decode_per_T(frn)
+        extras["decode_us_per_call"] = dec
+        t64 = dec["64"]["graph_us"] / 1e6
+        b64 = dec["64"]["bytes"]
+        ach = b64 / t64 / 1e9
+        roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(ach / hbm, 4), "traffic": None,
+                    "kernel": "frn_row_kernel<8, norm, cluster> at T=64 (the step's largest call)",
+                    "peak_kind": peak_kind}
+        large = [measure_rows(frn, 8, syn.sweep_tokens(m), "norm", 20000 + i, hbm)
+                 for i, m in enumerate((16 << 20, 32 << 20, 64 << 20))]
+        large.append(measure_rows(frn, 2, 8192, "quant_a", 30000, hbm, outlier=True, partial_std=1.0))
+        large.append(measure_rows(frn, 2, 8192, "quant_b", 31000, hbm, outlier=True, partial_std=1.0))
+        large.append(measure_rows(frn, 2, 8192, "norm", 32000, hbm, outlier=True, partial_std=1.0))
+        extras["large_T"] = large
+        extras["sweep"] = [dict(msg_bytes=m, **measure_rows(frn, 8, syn.sweep_tokens(m), "norm", 40000 + i, hbm))
+                           for i, m in enumerate(syn.SWEEP_BYTES)]
+        extras["quant_R4_T32_H4096"] = [measure_rows(frn, 4, 32, md, 50000, hbm, H=4096)
+                                        for md in ("quant_a", "quant_b")]
+
+    e2e_steps = min(args.steps, 2000)
+    t_e2e, h2d, d2h = measure_e2e(frn, e2e_steps)
+    t_e2e = max_over_ranks(t_e2e, world)
+    e2e = {"value": round(world * bytes_per_step * e2e_steps / t_e2e / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "ms_per_step": round(t_e2e / e2e_steps * 1e3, 4)}
+
+    cpu = cpu_baseline() if (rank == 0 and world == 1 and not args.no_extras) else None
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded torch.randn on device, bf16 inputs)",
+        "config": {"workload": WORKLOAD, "R": R_DEC, "H": H, "T": list(DECODE_T), "launch": "CUDA graph replay",
+                   "l2": f"{nsets} rotating input sets, {nsets * per_set / 1e6:.0f} MB > 2x L2 "
+                         f"({l2_bytes() / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
+        "frac_of_hbm": round(value / world / hbm, 4), "hbm_peak_gbs": hbm, "hbm_peak_kind": peak_kind,
+        "gpu_launches": args.steps * len(DECODE_T) * world,
+        "clocks": clocks, "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu, **extras,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * frn.h -- C ABI of libfrn: fused reduce + residual add + RMSNorm
+ * (+ per-group dynamic FP8 e4m3 quant) for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the tensor-parallel decoder-layer epilogue
+ * "allreduce -> residual add -> RMSNorm (-> per-1x128 FP8 quant)" re-posed for
+ * one GPU: the R per-rank partial hidden states already sit in this GPU's
+ * memory, and the "allreduce" is their fixed-order fp32 sum.
+ *
+ * Where it comes from:
+ *  - "ROCm AITER fused all-reduce + RMSNorm" (vLLM PR 37646 summary), sections
+ *    "implementation breakdown" (items 1-2) and "key source snippets"
+ *    (allreduce_rms_fusion.py, _aiter_ops.py): the replaced subgraph is
+ *    all_reduce(input) followed by rms_norm / fused_add_rms_norm, returning the
+ *    normalised activation and the un-normalised sum, and the fused op takes
+ *    (input, residual, weight, eps).
+ *  - "AMD fused AllReduce-RMSNorm quant kernel" (SGLang PR 24651 summary),
+ *    sections "features and motivation", "implementation breakdown" (items
+ *    1-3) and "key source snippets" (layernorm.py): the quant variant returns
+ *    ((fp8, scale), residual) or, with keep_bf16, ((bf16, fp8, scale), residual),
+ *    quantising the normalised bf16 activation per 1x128 group.
+ *  - "Fix: add missing end_sync barrier in fused allreduce+rmsnorm kernel"
+ *    (AITER PR 4346), "Pull request overview": a fused call must never read a
+ *    partial before its producer has finished, nor let the next call reuse
+ *    buffers the previous one still reads.  Here that is stream order: every
+ *    kernel starts with a grid-dependency wait before its first global access.
+ *
+ * Per token row t, with f32() the exact bf16 -> fp32 widening:
+ *   x_hat        = ((f32(P0[t]) + f32(P1[t])) + ... + f32(P[R-1][t])) + f32(residual[t])
+ *                  (fp32 adds, rank order 0..R-1, residual last)
+ *   residual_out = bf16_rn(x_hat)
+ *   x            = f32(residual_out)
+ *   y            = bf16_rn((x * rstd) * f32(gamma)),  rstd = 1/sqrt(sum(x^2)/H + eps)
+ *   per group g of group_size consecutive elements of y:
+ *     a = max |f32(y)|,  s = a / 448 (fp32),  q = e4m3fn_rn_satfinite(f32(y) / s),
+ *     and q = 0 when s == 0.
+ *
+ * residual_out is bit-exact (fixed-order fp32 sum, one round-to-nearest-even).
+ * y is within one bf16 ulp of the exact RMSNorm of residual_out: the sum of
+ * squares is an fp32 tree whose shape depends only on H, so a given row gives
+ * the same bits whatever T, launch shape or stream it is computed in.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are device memory (or memory the device can address), row-major,
+ *    rows contiguous: bf16 tensors are [T, H] with row stride H elements,
+ *    gamma is bf16 [H], q is e4m3fn bytes [T, H], scales is fp32 [T, H/group].
+ *    The library does not check the memory type; a host-only pointer faults.
+ *  - The caller owns every buffer.  The library allocates nothing, never
+ *    synchronises the host, and reads no device state on the host, so every
+ *    call can be captured in a CUDA graph.
+ *  - partials is a HOST array of R device pointers; it is read during the call
+ *    (copied into the kernel's parameters) and may be freed on return.
+ *    Partial pointers may repeat.
+ *  - residual may be NULL, which means a residual of zeros.  residual_out may
+ *    equal residual exactly (in-place update); any other overlap between an
+ *    output and any input, or between two outputs, is rejected.
+ *  - bf16 and fp8 pointers must be 16-byte aligned, scales 4-byte aligned.
+ *  - Limits: 1 <= R <= FRN_MAX_PARTIALS, T >= 0, H % 8 == 0,
+ *    8 <= H <= FRN_MAX_HIDDEN, eps finite >= 0, group_size == 128 with
+ *    H % 128 == 0.  T == 0 checks only the scalar arguments, touches no
+ *    pointer and returns FRN_OK.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    rejected call launches nothing.  FRN_ERR_CUDA reports a launch error;
+ *    errors of earlier, unrelated work on the stream are not reported here.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *    Work queued earlier on the stream (e.g. the producers of the partials)
+ *    is complete before the kernel reads anything; calls on different streams
+ *    that share buffers must be ordered by the caller (events).
+ */
+#ifndef FRN_H_
+#define FRN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, declared here so that callers need no
+ * CUDA header. */
+typedef struct CUstream_st* frn_stream_t;
+
+typedef enum frn_status {
+    FRN_OK = 0,
+    FRN_ERR_INVALID_ARG = 1,  /* NULL pointer, R < 1, T < 0, H < 1, bad eps, bad group, overlap */
+    FRN_ERR_UNSUPPORTED = 2,  /* well-formed but outside this build's limits            */
+    FRN_ERR_MISALIGNED = 3,   /* a tensor pointer breaks the alignment rule              */
+    FRN_ERR_CUDA = 4,         /* a CUDA runtime call or the kernel launch failed          */
+    FRN_ERR_TIMEOUT = 5       /* reserved for bounded device-side waits                   */
+} frn_status;
+
+#define FRN_MAX_PARTIALS 16
+#define FRN_MAX_HIDDEN 16384
+#define FRN_QUANT_GROUP 128
+#define FRN_E4M3_MAX 448.0f
+
+/*
+ * Sum R bf16 partials in fp32 (rank order), add the residual, write
+ * residual_out (bf16) and the RMSNorm output y (bf16).
+ *
+ *   partials     host array [R] of device pointers, each bf16 [T, H]
+ *   R            number of partials (tensor-parallel ranks), 1..16
+ *   residual     bf16 [T, H] or NULL (zeros)
+ *   gamma        bf16 [H] RMSNorm weight
+ *   residual_out bf16 [T, H] output (may equal residual)
+ *   y            bf16 [T, H] output
+ *   T, H         tokens and hidden size
+ *   eps          variance epsilon, added to mean(x^2) inside the square root
+ *   stream       CUDA stream
+ */
+frn_status fused_reduce_rmsnorm(const void* const* partials, int R,
+                                const void* residual, const void* gamma,
+                                void* residual_out, void* y,
+                                int64_t T, int H, float eps, frn_stream_t stream);
+
+/*
+ * As fused_reduce_rmsnorm, then per-group dynamic FP8 quant of y:
+ *
+ *   y        NULL -> variant A, outputs (fp8, scale) + residual_out and no bf16 y;
+ *            bf16 [T, H] -> variant B, outputs (bf16, fp8, scale) + residual_out.
+ *            q and scales are bit-identical between the two variants.
+ *   q_e4m3   e4m3fn [T, H] output codes (OCP FP8 E4M3: bias 7, max 448, no inf)
+ *   scales   fp32 [T, H / group_size] output, row-major; dequant = e4m3(q) * s
+ *   group_size  must be 128 (FRN_QUANT_GROUP)
+ */
+frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* partials, int R,
+                                                const void* residual, const void* gamma,
+                                                void* residual_out, void* y,
+                                                void* q_e4m3, float* scales,
+                                                int64_t T, int H, float eps, int group_size,
+                                                frn_stream_t stream);
+
+/* Static text for a status code. */
+const char* frn_status_string(frn_status s);
+
+/* Text describing the last error returned on the calling thread (argument name,
+ * CUDA error string), or "" if none.  Valid until the thread's next call. */
+const char* frn_last_error_detail(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int frn_version(void);
+
+/*
+ * Launch control.  Process-wide settings read at each call; set them before
+ * concurrent use, not while other threads are launching.
+ *
+ * frn_set_pdl: 1 (default) launches with programmatic dependent launch, so
+ *   the kernel's prologue may overlap the tail of the previous kernel on the
+ *   stream; the kernel still waits for that kernel's completion before its
+ *   first global-memory access.  0 launches plainly.
+ * frn_set_ctas_per_row: 0 (default) chooses the split of a row across a
+ *   thread-block cluster from T, H and the SM count; 1..8 forces it (rounded so
+ *   that no CTA is empty).  Results are bit-identical for every choice.
+ */
+frn_status frn_set_pdl(int enable);
+frn_status frn_set_ctas_per_row(int ctas_per_row);
+
+/*
+ * Report the launch shape a call with these sizes would use on the current
+ * device: CTAs per row (cluster size), threads per CTA, and CTAs in the grid.
+ * Any output pointer may be NULL.
+ */
+frn_status frn_query_launch(int64_t T, int H, int R, int quant,
+                            int* ctas_per_row, int* threads_per_cta, int64_t* grid_ctas);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FRN_H_ */

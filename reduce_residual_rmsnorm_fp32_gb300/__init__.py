@@ -1,0 +1,222 @@
+"""Fused reduce + residual add + RMSNorm (+ per-group dynamic FP8) for GB300.
+
+Thin Python binding of ``libfrn.so`` (C ABI in ``include/frn.h``).  This module
+only marshals arguments -- tensor pointers, sizes, the stream -- and allocates
+outputs with torch when the caller does not pass them; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is missing, the first call raises.
+
+Entry points (same names as the C ABI):
+
+* ``fused_reduce_rmsnorm(partials, residual, gamma, eps)`` -> ``(y, residual_out)``
+  -- the pair the replaced all_reduce -> rms_norm subgraph returns
+  ("ROCm AITER fused all-reduce + RMSNorm", vLLM PR 37646 summary).
+* ``fused_reduce_rmsnorm_quant_per_group(..., group_size=128, emit_bf16=False)``
+  -> ``((q, scales), residual_out)`` or, with ``emit_bf16``,
+  ``((y, q, scales), residual_out)`` -- the output contract of the fused quant
+  path ("AMD fused AllReduce-RMSNorm quant kernel", SGLang PR 24651 summary).
+
+``partials`` is a bf16 CUDA tensor ``[R, T, H]`` or a sequence of ``R`` bf16
+``[T, H]`` tensors (they need not be one allocation).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Sequence
+
+import torch
+
+__all__ = [
+    "FrnError", "fused_reduce_rmsnorm", "fused_reduce_rmsnorm_quant_per_group", "library",
+    "set_pdl", "set_ctas_per_row", "query_launch", "status_string", "version",
+    "FRN_OK", "FRN_ERR_INVALID_ARG", "FRN_ERR_UNSUPPORTED", "FRN_ERR_MISALIGNED", "FRN_ERR_CUDA",
+    "FRN_ERR_TIMEOUT", "MAX_PARTIALS", "MAX_HIDDEN", "QUANT_GROUP",
+]
+
+FRN_OK, FRN_ERR_INVALID_ARG, FRN_ERR_UNSUPPORTED, FRN_ERR_MISALIGNED, FRN_ERR_CUDA, FRN_ERR_TIMEOUT = range(6)
+MAX_PARTIALS = 16
+MAX_HIDDEN = 16384
+QUANT_GROUP = 128
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfrn.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class FrnError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        self.detail = detail
+        super().__init__(f"{status_string(status)}: {detail}")
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.fused_reduce_rmsnorm.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, i64, i32, f32, vp]
+    lib.fused_reduce_rmsnorm.restype = i32
+    lib.fused_reduce_rmsnorm_quant_per_group.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, vp, vp,
+                                                         i64, i32, f32, i32, vp]
+    lib.fused_reduce_rmsnorm_quant_per_group.restype = i32
+    lib.frn_status_string.argtypes = [i32]
+    lib.frn_status_string.restype = ctypes.c_char_p
+    lib.frn_last_error_detail.argtypes = []
+    lib.frn_last_error_detail.restype = ctypes.c_char_p
+    lib.frn_version.argtypes = []
+    lib.frn_version.restype = i32
+    lib.frn_set_pdl.argtypes = [i32]
+    lib.frn_set_pdl.restype = i32
+    lib.frn_set_ctas_per_row.argtypes = [i32]
+    lib.frn_set_ctas_per_row.restype = i32
+    lib.frn_query_launch.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                     ctypes.POINTER(i64)]
+    lib.frn_query_launch.restype = i32
+    return lib
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libfrn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"libfrn.so not found at {LIB_PATH}; build it with "
+                        "`python -m reduce_residual_rmsnorm_fp32_gb300._build` (needs nvcc)")
+                _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().frn_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(library().frn_version())
+
+
+def _check(status: int) -> None:
+    if status != FRN_OK:
+        raise FrnError(status, library().frn_last_error_detail().decode())
+
+
+def set_pdl(enable: bool) -> None:
+    _check(library().frn_set_pdl(1 if enable else 0))
+
+
+def set_ctas_per_row(n: int) -> None:
+    _check(library().frn_set_ctas_per_row(int(n)))
+
+
+def query_launch(T: int, H: int, R: int, quant: bool = False) -> tuple[int, int, int]:
+    c, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    _check(library().frn_query_launch(int(T), int(H), int(R), int(bool(quant)), ctypes.byref(c),
+                                      ctypes.byref(t), ctypes.byref(g)))
+    return c.value, t.value, g.value
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, device: torch.device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device or t.device.type != "cuda":
+        raise ValueError(f"{name} must be on {device} (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _partials(partials) -> tuple[list[int], int, int, int, torch.device]:
+    if isinstance(partials, torch.Tensor):
+        if partials.dim() != 3:
+            raise ValueError("stacked partials must be [R, T, H]")
+        R, T, H = partials.shape
+        dev = partials.device
+        _check_tensor(partials, "partials", torch.bfloat16, (R, T, H), dev)
+        base, step = partials.data_ptr(), T * H * 2
+        return [base + r * step for r in range(R)], R, T, H, dev
+    parts = list(partials)
+    if not parts:
+        raise ValueError("partials is empty")
+    T, H = parts[0].shape
+    dev = parts[0].device
+    for i, p in enumerate(parts):
+        _check_tensor(p, f"partials[{i}]", torch.bfloat16, (T, H), dev)
+    return [p.data_ptr() for p in parts], len(parts), T, H, dev
+
+
+def _stream(stream, device) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def fused_reduce_rmsnorm(partials: torch.Tensor | Sequence[torch.Tensor], residual: torch.Tensor | None,
+                         gamma: torch.Tensor, eps: float = 1e-6, *, residual_out: torch.Tensor | None = None,
+                         y: torch.Tensor | None = None, stream=None):
+    """Returns ``(y, residual_out)``.  ``residual_out`` may be ``residual`` (in place)."""
+    ptrs, R, T, H, dev = _partials(partials)
+    if residual is not None:
+        _check_tensor(residual, "residual", torch.bfloat16, (T, H), dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
+    if residual_out is None:
+        residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
+    _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
+    arr = (ctypes.c_void_p * R)(*ptrs)
+    with torch.cuda.device(dev):
+        st = library().fused_reduce_rmsnorm(arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y),
+                                            T, H, float(eps), _stream(stream, dev))
+    _check(st)
+    return y, residual_out
+
+
+def fused_reduce_rmsnorm_quant_per_group(partials, residual: torch.Tensor | None, gamma: torch.Tensor,
+                                         eps: float = 1e-6, group_size: int = QUANT_GROUP,
+                                         emit_bf16: bool = False, *, residual_out: torch.Tensor | None = None,
+                                         y: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                                         scales: torch.Tensor | None = None, stream=None):
+    """Returns ``((q, scales), residual_out)``, or ``((y, q, scales), residual_out)`` when
+    ``emit_bf16`` (or when ``y`` is given).  ``q`` is float8_e4m3fn ``[T, H]``, ``scales``
+    float32 ``[T, H // group_size]``."""
+    ptrs, R, T, H, dev = _partials(partials)
+    if residual is not None:
+        _check_tensor(residual, "residual", torch.bfloat16, (T, H), dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
+    if group_size < 1 or H % group_size:
+        raise ValueError(f"group_size={group_size} must divide H={H}")
+    emit_bf16 = emit_bf16 or y is not None
+    if residual_out is None:
+        residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if emit_bf16 and y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if q is None:
+        q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=dev)
+    if scales is None:
+        scales = torch.empty((T, H // group_size), dtype=torch.float32, device=dev)
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
+    if y is not None:
+        _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
+    if q.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError("q must be float8_e4m3fn or uint8")
+    _check_tensor(q, "q", q.dtype, (T, H), dev)
+    _check_tensor(scales, "scales", torch.float32, (T, H // group_size), dev)
+    arr = (ctypes.c_void_p * R)(*ptrs)
+    with torch.cuda.device(dev):
+        st = library().fused_reduce_rmsnorm_quant_per_group(
+            arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales),
+            T, H, float(eps), int(group_size), _stream(stream, dev))
+    _check(st)
+    if emit_bf16:
+        return (y, q, scales), residual_out
+    return (q, scales), residual_out

@@ -141,3 +141,28 @@ def algorithmic_bytes(R: int, T: int, H: int, mode: str = "norm", group_size: in
     else:
         raise ValueError(mode)
     return b
+
+
+def make_inputs_device(R: int, T: int, H: int, seed: int = 0, partial_std: float = 1.0,
+                       residual_std: float = 1.0, gamma_lo: float = 0.5, gamma_hi: float = 1.5,
+                       outlier_frac: float = 0.0, outlier_scale: float = 50.0, device="cuda"):
+    """Same distributions and draw order as ``make_inputs``, drawn on the device with
+    a seeded torch generator (a different random stream from the numpy one).  Used
+    for large benchmark inputs that are never compared with the oracle.
+
+    Returns bf16 device tensors (partials [R,T,H], residual [T,H], gamma [H]).
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    p = torch.randn((R, T, H), generator=g, device=device, dtype=torch.float32)
+    if partial_std != 1.0:
+        p.mul_(partial_std)
+    res = torch.randn((T, H), generator=g, device=device, dtype=torch.float32)
+    if residual_std != 1.0:
+        res.mul_(residual_std)
+    gamma = torch.rand((H,), generator=g, device=device, dtype=torch.float32) * (gamma_hi - gamma_lo) + gamma_lo
+    if outlier_frac > 0.0:
+        n_out = int(round(outlier_frac * H))
+        chans = torch.randperm(H, generator=g, device=device)[:n_out]
+        p[:, :, chans] *= outlier_scale
+    return p.to(torch.bfloat16), res.to(torch.bfloat16), gamma.to(torch.bfloat16)

@@ -1,0 +1,227 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Covers the five workloads (small case; decode T in {8,16,32,64}; quant R=4
+T=32 H=4096 in both output variants; the message-size sweep at H=7168 with
+sampled rows at the large sizes; the prefill chunk with outlier channels),
+random shapes with ragged tails, and the edge cases: R=1, R=16, H=8, H=16384,
+NULL residual, in-place residual, zero rows, huge and tiny magnitudes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reduce_residual_rmsnorm_fp32_gb300 as frn
+from reduce_residual_rmsnorm_fp32_gb300 import synthetic as syn
+from frn_testlib import (DevInputs, assert_quant_close, assert_residual_exact, assert_y_close, gpu_norm,
+                         gpu_quant, host_bits, dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+ORC = None
+THREADS = 8
+
+
+def orc():
+    global ORC
+    if ORC is None:
+        ORC = oracle.Oracle()
+    return ORC
+
+
+def ref_norm(inp):
+    return orc().reduce_rmsnorm(inp.partials, inp.residual, inp.gamma, inp.eps, threads=THREADS)
+
+
+def ref_quant(inp):
+    return orc().reduce_rmsnorm_quant(inp.partials, inp.residual, inp.gamma, inp.eps, 128, threads=THREADS)
+
+
+def check_norm(inp, what, rows=None):
+    d = DevInputs(inp)
+    ro, y = gpu_norm(d)
+    if rows is not None:
+        sub = syn.Inputs(inp.partials[:, rows], None if inp.residual is None else inp.residual[rows],
+                         inp.gamma, inp.eps)
+        rro, ry = ref_norm(sub)
+        ro, y = ro[rows], y[rows]
+    else:
+        rro, ry = ref_norm(inp)
+    assert_residual_exact(ro, rro, what)
+    return assert_y_close(y, ry, what)
+
+
+def check_quant(inp, what, rows=None):
+    d = DevInputs(inp)
+    roA, _, qA, sA = gpu_quant(d, emit_bf16=False)
+    roB, yB, qB, sB = gpu_quant(d, emit_bf16=True)
+    ro_n, y_n = gpu_norm(d)
+    # the two variants agree bit for bit, and B's y is the plain entry point's y
+    assert np.array_equal(qA, qB) and np.array_equal(sA.view(np.uint32), sB.view(np.uint32)), what
+    assert np.array_equal(roA, roB) and np.array_equal(roA, ro_n), what
+    assert np.array_equal(yB, y_n), what
+    if rows is not None:
+        sub = syn.Inputs(inp.partials[:, rows], None if inp.residual is None else inp.residual[rows],
+                         inp.gamma, inp.eps)
+        rro, ry, rq, rs = ref_quant(sub)
+        roB, yB, qB, sB = roB[rows], yB[rows], qB[rows], sB[rows]
+    else:
+        rro, ry, rq, rs = ref_quant(inp)
+    assert_residual_exact(roB, rro, what)
+    assert_y_close(yB, ry, what)
+    return assert_quant_close(yB, qB, sB, ry, rq, rs, what)
+
+
+def sample_rows(T, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    rows.update({0, T - 1})
+    return np.array(sorted(rows))
+
+
+# ------------------------------------------------------------- workloads --
+
+def test_small_case():
+    check_norm(syn.config_small(), "R=2 T=4 H=256")
+
+
+@pytest.mark.parametrize("T", syn.DECODE_TOKENS)
+def test_decode(T):
+    check_norm(syn.config_decode(T), f"decode T={T}")
+
+
+def test_quant_both_variants():
+    check_quant(syn.config_quant(), "quant R=4 T=32 H=4096")
+
+
+@pytest.mark.parametrize("msg", syn.SWEEP_BYTES)
+def test_sweep(msg):
+    T = syn.sweep_tokens(msg)
+    inp = syn.config_sweep(msg)
+    rows = sample_rows(T) if T > 600 else None
+    check_norm(inp, f"sweep {msg} B (T={T})", rows)
+
+
+def test_prefill_outliers_quant():
+    inp = syn.config_prefill()
+    assert inp.outlier_channels.size == 72
+    stats = check_quant(inp, "prefill R=2 T=8192 H=7168", rows=sample_rows(inp.T, 64))
+    # properties that hold at every row: each nonzero group reaches |q| = 448,
+    # and the scales are the GPU's own absmax(y)/448
+    d = DevInputs(inp)
+    (y, q, s), _ = frn.fused_reduce_rmsnorm_quant_per_group(d.partials, d.residual, d.gamma, d.eps, 128, True)
+    qf = q.view(torch.float8_e4m3fn).float().abs().view(inp.T, 56, 128)
+    assert torch.all(qf.amax(-1)[s > 0] == 448.0)
+    ya = y.float().abs().view(inp.T, 56, 128).amax(-1).cpu().numpy()
+    assert np.array_equal(s.cpu().numpy(), ya / np.float32(448.0))
+    # groups holding an outlier channel carry far larger scales than the rest
+    outg = np.unique(inp.outlier_channels // 128)
+    sn = s.cpu().numpy()
+    rest = np.setdiff1d(np.arange(56), outg)
+    if rest.size:
+        assert np.median(sn[:, outg]) > 5 * np.median(sn[:, rest])
+    assert stats["code_mismatch_frac"] <= 1e-3
+
+
+# ----------------------------------------------------------- random shapes --
+
+SHAPES = [
+    (1, 1, 8), (1, 3, 24), (2, 7, 136), (3, 33, 1000), (5, 2, 2048), (8, 5, 7168), (13, 9, 4096),
+    (16, 4, 7168), (2, 300, 256), (4, 17, 8200), (3, 3, 16384), (16, 2, 16384), (7, 65, 520),
+    (2, 129, 7168), (1, 1025, 4096),
+]
+
+
+@pytest.mark.parametrize("R,T,H", SHAPES)
+@pytest.mark.parametrize("with_residual", [True, False])
+def test_random_shapes_norm(R, T, H, with_residual):
+    inp = syn.make_inputs(R, T, H, seed=R * 1000 + T + H, with_residual=with_residual)
+    check_norm(inp, f"R={R} T={T} H={H} res={with_residual}")
+
+
+@pytest.mark.parametrize("R,T,H", [s for s in SHAPES if s[2] % 128 == 0])
+def test_random_shapes_quant(R, T, H):
+    inp = syn.make_inputs(R, T, H, seed=7 + R * 1000 + T + H, partial_std=0.5)
+    check_quant(inp, f"quant R={R} T={T} H={H}")
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 4, 5, 7, 8])
+def test_forced_cluster_split_is_bit_identical(ctas):
+    """Whatever number of CTAs a row is split over, every output has the same bits."""
+    inp = syn.make_inputs(8, 11, 7168, seed=5, partial_std=0.5)
+    d = DevInputs(inp)
+    base = gpu_quant(d, True)
+    try:
+        frn.set_ctas_per_row(ctas)
+        got = gpu_quant(d, True)
+    finally:
+        frn.set_ctas_per_row(0)
+    for a, b in zip(base, got):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
+# ------------------------------------------------------------- edge cases --
+
+def test_empty_T_is_noop():
+    d = DevInputs(syn.make_inputs(2, 1, 256))
+    p = d.partials[:, :0]
+    ro = torch.full((0, 256), 1.0, dtype=torch.bfloat16, device="cuda")
+    y, ro2 = frn.fused_reduce_rmsnorm([p[0], p[1]], None, d.gamma, 1e-6, residual_out=ro)
+    assert y.shape == (0, 256) and ro2 is ro
+    frn.fused_reduce_rmsnorm_quant_per_group([p[0], p[1]], None, d.gamma, 1e-6)
+    torch.cuda.synchronize()
+
+
+def test_in_place_residual():
+    inp = syn.make_inputs(4, 19, 4096, seed=3)
+    d = DevInputs(inp)
+    rro, ry = ref_norm(inp)
+    res = d.residual.clone()
+    y, ro = frn.fused_reduce_rmsnorm(d.partials, res, d.gamma, inp.eps, residual_out=res)
+    assert ro.data_ptr() == res.data_ptr()
+    assert_residual_exact(host_bits(res), rro, "in place")
+    assert_y_close(host_bits(y), ry, "in place")
+
+
+def test_separate_partial_allocations_and_repeats():
+    """Partials as R separate tensors, including one pointer passed twice."""
+    inp = syn.make_inputs(3, 9, 2048, seed=4)
+    parts = [dev_bf16(inp.partials[r]) for r in range(3)]
+    rep = np.stack([inp.partials[0], inp.partials[1], inp.partials[2], inp.partials[1]])
+    rro, ry = orc().reduce_rmsnorm(rep, inp.residual, inp.gamma, inp.eps)
+    y, ro = frn.fused_reduce_rmsnorm([parts[0], parts[1], parts[2], parts[1]], dev_bf16(inp.residual),
+                                     dev_bf16(inp.gamma), inp.eps)
+    assert_residual_exact(host_bits(ro), rro)
+    assert_y_close(host_bits(y), ry)
+
+
+def test_zero_rows_and_zero_groups():
+    inp = syn.make_inputs(2, 6, 1024, seed=6)
+    inp.partials[:, 2] = 0
+    inp.residual[2] = 0
+    inp.partials[:, 4, 128:256] = 0
+    inp.residual[4, 128:256] = 0
+    stats = check_quant(inp, "zero rows")
+    d = DevInputs(inp)
+    _, _, q, s = gpu_quant(d, True)
+    assert np.all(q[2] == 0) and np.all(s[2] == 0)
+    assert s[4, 1] == 0 and np.all(q[4, 128:256] == 0)
+    assert stats["absmax_flips"] <= 2
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -60, 2.0 ** -20, 2.0 ** 20, 2.0 ** 50])
+def test_magnitudes(scale):
+    """Rows far from unit scale, within the range where fp32 sums of squares of a
+    16384-wide row stay finite and normal."""
+    inp = syn.make_inputs(3, 5, 4096, seed=8)
+    f = syn.bf16_bits_to_f32(inp.partials) * np.float32(scale)
+    r = syn.bf16_bits_to_f32(inp.residual) * np.float32(scale)
+    inp = syn.Inputs(syn.f32_to_bf16_bits(f), syn.f32_to_bf16_bits(r), inp.gamma, 1e-30)
+    check_quant(inp, f"scale {scale}")
+
+
+def test_eps_matters():
+    """Rows whose mean square is comparable to eps."""
+    inp = syn.make_inputs(2, 8, 2048, seed=9, partial_std=1e-3, residual_std=1e-3)
+    check_norm(syn.Inputs(inp.partials, inp.residual, inp.gamma, 1e-6), "eps ~ mean square")
+    check_norm(syn.Inputs(inp.partials, inp.residual, inp.gamma, 0.5), "eps dominant")

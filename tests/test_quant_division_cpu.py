@@ -1,0 +1,50 @@
+"""The quant epilogue divides y by the group scale with one correctly rounded
+reciprocal per group and one FMA correction step (Markstein's theorem) instead
+of an IEEE divide per element.  This CPU test replays that sequence in exact
+rational arithmetic for every bf16 significand of y against every significand
+the scale s = RN(absmax / 448) can take (absmax is a bf16), and checks that it
+always equals the correctly rounded quotient RN(y / s).  Powers of two scale
+the operands exactly (the kernel takes this path only for s >= 2^-64, where no
+intermediate underflows or overflows), so these pairs cover every case."""
+import math
+from fractions import Fraction as F
+
+
+def rn32(x: F) -> F:
+    """Round a rational to the nearest fp32 value, ties to even (normal range)."""
+    if x == 0:
+        return F(0)
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = math.floor(math.log2(a.numerator) - math.log2(a.denominator))
+    while F(2) ** e > a:
+        e -= 1
+    while F(2) ** (e + 1) <= a:
+        e += 1
+    ulp = F(2) ** (e - 23)
+    n = a / ulp
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > F(1, 2) or (rem == F(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * fl * ulp
+
+
+def test_fma_corrected_quotient_is_correctly_rounded():
+    y_sigs = [F(128 + m, 128) for m in range(128)]          # bf16 significands in [1, 2)
+    s_sigs = set()
+    for m in y_sigs:
+        s = rn32(m / 448)
+        while s >= 2:
+            s /= 2
+        while s < 1:
+            s *= 2
+        s_sigs.add(s)
+    assert len(s_sigs) == 128
+    for s in s_sigs:
+        rs = rn32(1 / s)                                   # __frcp_rn
+        for y in y_sigs:
+            q0 = rn32(y * rs)                              # __fmul_rn
+            rem = rn32(y - s * q0)                         # __fmaf_rn(-s, q0, y)
+            q1 = rn32(q0 + rem * rs)                       # __fmaf_rn(rem, rs, q0)
+            assert q1 == rn32(y / s), (y, s)
