@@ -294,6 +294,43 @@ def measure_rows(frn, R, T, mode, seed, hbm, outlier=False, partial_std=0.5, H=H
             "GBps": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "input_sets": n}
 
 
+def measure_fusion(frn, R, T, Hh, seed, hbm, outlier=False, partial_std=0.5):
+    """1-kernel (fused) vs 2-kernel vs 3-kernel quant epilogue (variant B), same
+    inputs, cold L2: device time per call and what fusion saves."""
+    fp = syn.algorithmic_bytes(R, T, Hh, "quant_b")
+    n = sets_to_beat_l2(fp)
+    sets = []
+    for k in range(n):
+        p, r, g = syn.make_inputs_device(R, T, Hh, seed=seed + k, partial_std=partial_std,
+                                         outlier_frac=0.01 if outlier else 0.0)
+        sets.append((p, r, g, torch.empty((T, Hh), dtype=torch.bfloat16, device="cuda"),
+                     torch.empty((T, Hh), dtype=torch.bfloat16, device="cuda"),
+                     torch.empty((T, Hh), dtype=torch.float8_e4m3fn, device="cuda"),
+                     torch.empty((T, Hh // 128), dtype=torch.float32, device="cuda")))
+    ws = torch.empty((max(frn.unfused_workspace_bytes(T, Hh, 3, True, True), 16),), dtype=torch.uint8,
+                     device="cuda")
+    out = {"R": R, "T": T, "H": Hh, "bytes_fused": fp}
+    for name, stages in (("fused_1_kernel", 1), ("unfused_2_kernels", 2), ("unfused_3_kernels", 3)):
+        def body(stages=stages):
+            for p, r, g, ro, y, q, s in sets:
+                if stages == 1:
+                    frn.fused_reduce_rmsnorm_quant_per_group(p, r, g, EPS, 128, True, residual_out=ro, y=y, q=q,
+                                                             scales=s)
+                else:
+                    frn.unfused_reduce_rmsnorm(p, r, g, EPS, stages=stages, quant=True, emit_bf16=True,
+                                               workspace=ws, residual_out=ro, y=y, q=q, scales=s)
+        gr = capture(body)
+        t = time_graph(gr, n, min_seconds=0.1)
+        out[name + "_us"] = round(t * 1e6, 2)
+        del gr
+    out["speedup_vs_2"] = round(out["unfused_2_kernels_us"] / out["fused_1_kernel_us"], 3)
+    out["speedup_vs_3"] = round(out["unfused_3_kernels_us"] / out["fused_1_kernel_us"], 3)
+    out["fused_GBps"] = round(fp / (out["fused_1_kernel_us"] * 1e-6) / 1e9, 1)
+    del sets, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_e2e(frn, steps: int):
     """The decode step through the public API from pinned host buffers."""
     host = {}
@@ -492,6 +529,9 @@ def main():
                            for i, m in enumerate(syn.SWEEP_BYTES)]
         extras["quant_R4_T32_H4096"] = [measure_rows(frn, 4, 32, md, 50000, hbm, H=4096)
                                         for md in ("quant_a", "quant_b")]
+        extras["fusion_gain"] = [measure_fusion(frn, 4, 32, 4096, 60000, hbm),
+                                 measure_fusion(frn, 8, 64, H, 61000, hbm),
+                                 measure_fusion(frn, 2, 8192, H, 62000, hbm, outlier=True, partial_std=1.0)]
 
     e2e_steps = min(args.steps, 2000)
     t_e2e, h2d, d2h = measure_e2e(frn, e2e_steps)

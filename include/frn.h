@@ -86,7 +86,7 @@ typedef enum frn_status {
     FRN_ERR_UNSUPPORTED = 2,  /* well-formed but outside this build's limits            */
     FRN_ERR_MISALIGNED = 3,   /* a tensor pointer breaks the alignment rule              */
     FRN_ERR_CUDA = 4,         /* a CUDA runtime call or the kernel launch failed          */
-    FRN_ERR_TIMEOUT = 5       /* reserved for bounded device-side waits                   */
+    FRN_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out (frn_device_status)  */
 } frn_status;
 
 #define FRN_MAX_PARTIALS 16
@@ -130,6 +130,35 @@ frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* partials, int
                                                 int64_t T, int H, float eps, int group_size,
                                                 frn_stream_t stream);
 
+/*
+ * Unfused comparison paths: the same outputs, bit for bit, computed the way an
+ * unfused layer would, to measure what fusion saves ("AMD fused
+ * AllReduce-RMSNorm quant kernel", SGLang PR 24651 summary, implementation
+ * breakdown items 2 and 4: the 3-kernel / 2-kernel / 1-kernel comparison).
+ *
+ *   q_e4m3 == NULL and scales == NULL: no quant; stages must be 2
+ *       (reduce -> residual add + RMSNorm).
+ *   otherwise: per-group quant as fused_reduce_rmsnorm_quant_per_group
+ *       (y NULL = variant A), stages 3 (reduce -> residual add + RMSNorm ->
+ *       quant) or 2 (fused reduce + add + RMSNorm -> stand-alone quant).
+ *
+ * The reduce stage writes the fp32 sum of the partials to the workspace; a quant
+ * path without a y output keeps the bf16 y there.  workspace: device memory of
+ * at least frn_unfused_workspace_bytes(T, H, stages, quant, emit_y) bytes,
+ * 16-byte aligned, not overlapping any argument; the caller owns it and it may
+ * be reused once the call's work on `stream` has completed.  Other arguments,
+ * conventions and errors as for the fused entry points.
+ */
+int64_t frn_unfused_workspace_bytes(int64_t T, int H, int stages, int quant, int emit_y);
+
+frn_status frn_unfused_reduce_rmsnorm(const void* const* partials, int R,
+                                      const void* residual, const void* gamma,
+                                      void* residual_out, void* y,
+                                      void* q_e4m3, float* scales,
+                                      int64_t T, int H, float eps, int group_size,
+                                      int stages, void* workspace, int64_t workspace_bytes,
+                                      frn_stream_t stream);
+
 /* Static text for a status code. */
 const char* frn_status_string(frn_status s);
 
@@ -142,26 +171,51 @@ int frn_version(void);
 
 /*
  * Launch control.  Process-wide settings read at each call; set them before
- * concurrent use, not while other threads are launching.
+ * concurrent use, not while other threads are launching.  Results are
+ * bit-identical for every choice.
  *
  * frn_set_pdl: 1 (default) launches with programmatic dependent launch, so
  *   the kernel's prologue may overlap the tail of the previous kernel on the
  *   stream; the kernel still waits for that kernel's completion before its
  *   first global-memory access.  0 launches plainly.
- * frn_set_ctas_per_row: 0 (default) chooses the split of a row across a
- *   thread-block cluster from T, H and the SM count; 1..8 forces it (rounded so
- *   that no CTA is empty).  Results are bit-identical for every choice.
+ * frn_set_kernel: 0 (default) picks the kernel from T and the SM count;
+ *   1 forces the row kernel (one row per thread-block cluster, for few rows),
+ *   2 forces the stream kernel (persistent, one CTA per SM, rows streamed
+ *   through shared memory with TMA bulk copies, for many rows).
+ * frn_set_ctas_per_row: row kernel only.  0 (default) chooses how many CTAs
+ *   of a cluster share a row from T, H and the SM count; 1..8 forces it
+ *   (rounded so that no CTA is empty).
  */
 frn_status frn_set_pdl(int enable);
+frn_status frn_set_kernel(int kernel);
 frn_status frn_set_ctas_per_row(int ctas_per_row);
 
 /*
- * Report the launch shape a call with these sizes would use on the current
- * device: CTAs per row (cluster size), threads per CTA, and CTAs in the grid.
- * Any output pointer may be NULL.
+ * Report the launch a call with these sizes would use on the current device:
+ * kernel (1 row, 2 stream), CTAs per row (cluster size; 1 for the stream
+ * kernel), threads per CTA, and CTAs in the grid.  Output pointers may be NULL.
  */
-frn_status frn_query_launch(int64_t T, int H, int R, int quant,
-                            int* ctas_per_row, int* threads_per_cta, int64_t* grid_ctas);
+frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int* ctas_per_row,
+                            int* threads_per_cta, int64_t* grid_ctas);
+
+/*
+ * Device-side failure detection.  The stream kernel bounds every wait on its
+ * shared-memory pipeline (default 2 s).  A wait that runs out makes the kernel
+ * stop early and set a status word on the device; the call's outputs are then
+ * incomplete.  frn_device_status reads that word for the current device --
+ * synchronously, so call it after the work in question has completed (e.g.
+ * after synchronising its stream) -- and returns FRN_ERR_TIMEOUT if it is set
+ * (FRN_OK otherwise).  clear != 0 resets the word.
+ */
+frn_status frn_device_status(int clear);
+
+/*
+ * Test hook for the failure path above.  inject_stall != 0 makes every CTA of
+ * the stream kernel skip its first bulk copy, so that the consumers' wait on it
+ * runs out; wait_limit_ns > 0 replaces the 2 s bound (<= 0 restores it).  The
+ * kernel then returns with the status word set and the context stays usable.
+ */
+frn_status frn_set_test_hooks(int inject_stall, int64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -30,12 +30,15 @@ import torch
 
 __all__ = [
     "FrnError", "fused_reduce_rmsnorm", "fused_reduce_rmsnorm_quant_per_group", "library",
-    "set_pdl", "set_ctas_per_row", "query_launch", "status_string", "version",
+    "set_pdl", "set_kernel", "set_ctas_per_row", "query_launch", "device_status", "set_test_hooks",
+    "status_string", "version", "KERNEL_AUTO", "KERNEL_ROWS", "KERNEL_STREAM",
+    "unfused_workspace_bytes", "unfused_reduce_rmsnorm",
     "FRN_OK", "FRN_ERR_INVALID_ARG", "FRN_ERR_UNSUPPORTED", "FRN_ERR_MISALIGNED", "FRN_ERR_CUDA",
     "FRN_ERR_TIMEOUT", "MAX_PARTIALS", "MAX_HIDDEN", "QUANT_GROUP",
 ]
 
 FRN_OK, FRN_ERR_INVALID_ARG, FRN_ERR_UNSUPPORTED, FRN_ERR_MISALIGNED, FRN_ERR_CUDA, FRN_ERR_TIMEOUT = range(6)
+KERNEL_AUTO, KERNEL_ROWS, KERNEL_STREAM = 0, 1, 2
 MAX_PARTIALS = 16
 MAX_HIDDEN = 16384
 QUANT_GROUP = 128
@@ -69,9 +72,20 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_set_pdl.restype = i32
     lib.frn_set_ctas_per_row.argtypes = [i32]
     lib.frn_set_ctas_per_row.restype = i32
+    lib.frn_set_kernel.argtypes = [i32]
+    lib.frn_set_kernel.restype = i32
     lib.frn_query_launch.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
-                                     ctypes.POINTER(i64)]
+                                     ctypes.POINTER(i32), ctypes.POINTER(i64)]
     lib.frn_query_launch.restype = i32
+    lib.frn_device_status.argtypes = [i32]
+    lib.frn_device_status.restype = i32
+    lib.frn_set_test_hooks.argtypes = [i32, i64]
+    lib.frn_set_test_hooks.restype = i32
+    lib.frn_unfused_workspace_bytes.argtypes = [i64, i32, i32, i32, i32]
+    lib.frn_unfused_workspace_bytes.restype = i64
+    lib.frn_unfused_reduce_rmsnorm.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, vp, vp, i64, i32, f32, i32,
+                                               i32, vp, i64, vp]
+    lib.frn_unfused_reduce_rmsnorm.restype = i32
     return lib
 
 
@@ -110,11 +124,26 @@ def set_ctas_per_row(n: int) -> None:
     _check(library().frn_set_ctas_per_row(int(n)))
 
 
-def query_launch(T: int, H: int, R: int, quant: bool = False) -> tuple[int, int, int]:
-    c, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
-    _check(library().frn_query_launch(int(T), int(H), int(R), int(bool(quant)), ctypes.byref(c),
+def set_kernel(kind: int) -> None:
+    """KERNEL_AUTO (default), KERNEL_ROWS or KERNEL_STREAM."""
+    _check(library().frn_set_kernel(int(kind)))
+
+
+def query_launch(T: int, H: int, R: int, quant: bool = False) -> tuple[int, int, int, int]:
+    """(kernel, ctas_per_row, threads_per_cta, grid_ctas) a call would use on the current device."""
+    k, c, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    _check(library().frn_query_launch(int(T), int(H), int(R), int(bool(quant)), ctypes.byref(k), ctypes.byref(c),
                                       ctypes.byref(t), ctypes.byref(g)))
-    return c.value, t.value, g.value
+    return k.value, c.value, t.value, g.value
+
+
+def device_status(clear: bool = False) -> int:
+    """FRN_OK, or FRN_ERR_TIMEOUT if a bounded device-side wait ran out (synchronous read)."""
+    return int(library().frn_device_status(1 if clear else 0))
+
+
+def set_test_hooks(inject_stall: bool = False, wait_limit_ns: int = 0) -> None:
+    _check(library().frn_set_test_hooks(1 if inject_stall else 0, int(wait_limit_ns)))
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -218,5 +247,54 @@ def fused_reduce_rmsnorm_quant_per_group(partials, residual: torch.Tensor | None
             T, H, float(eps), int(group_size), _stream(stream, dev))
     _check(st)
     if emit_bf16:
+        return (y, q, scales), residual_out
+    return (q, scales), residual_out
+
+
+def unfused_workspace_bytes(T: int, H: int, stages: int, quant: bool, emit_y: bool) -> int:
+    return int(library().frn_unfused_workspace_bytes(int(T), int(H), int(stages), int(bool(quant)),
+                                                     int(bool(emit_y))))
+
+
+def unfused_reduce_rmsnorm(partials, residual: torch.Tensor | None, gamma: torch.Tensor, eps: float = 1e-6, *,
+                           stages: int = 2, quant: bool = False, emit_bf16: bool = True,
+                           group_size: int = QUANT_GROUP, workspace: torch.Tensor | None = None,
+                           residual_out: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                           q: torch.Tensor | None = None, scales: torch.Tensor | None = None, stream=None):
+    """The unfused comparison paths (same bits as the fused entry points).
+
+    Without quant returns ``(y, residual_out)``; with quant returns like
+    ``fused_reduce_rmsnorm_quant_per_group``.  ``workspace`` is a CUDA uint8
+    tensor of at least ``unfused_workspace_bytes(...)`` bytes (allocated here
+    when not given)."""
+    ptrs, R, T, H, dev = _partials(partials)
+    if residual is not None:
+        _check_tensor(residual, "residual", torch.bfloat16, (T, H), dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
+    emit_y = (not quant) or emit_bf16 or y is not None
+    need = unfused_workspace_bytes(T, H, stages, quant, emit_y)
+    if need < 0:
+        raise ValueError(f"stages={stages} needs quant" if stages == 3 else f"stages={stages} must be 2 or 3")
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    if residual_out is None:
+        residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if emit_y and y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if quant:
+        if q is None:
+            q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=dev)
+        if scales is None:
+            scales = torch.empty((T, H // group_size), dtype=torch.float32, device=dev)
+    arr = (ctypes.c_void_p * R)(*ptrs)
+    with torch.cuda.device(dev):
+        st = library().frn_unfused_reduce_rmsnorm(
+            arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q) if quant else None,
+            _ptr(scales) if quant else None, T, H, float(eps), int(group_size), int(stages), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream, dev))
+    _check(st)
+    if not quant:
+        return y, residual_out
+    if emit_y:
         return (y, q, scales), residual_out
     return (q, scales), residual_out

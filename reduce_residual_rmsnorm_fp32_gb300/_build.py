@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfrn.so")
-SOURCES = ["frn_api.cu", "frn_launch_norm.cu", "frn_launch_quant_a.cu", "frn_launch_quant_b.cu"]
+SOURCES = ["frn_api.cu", "frn_launch_norm.cu", "frn_launch_quant_a.cu", "frn_launch_quant_b.cu",
+           "frn_launch_unfused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-Xcompiler", "-Wall"]

@@ -25,9 +25,16 @@ namespace {
 thread_local char g_detail[256] = "";
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_force_ctas{0};
+std::atomic<int> g_force_kernel{0};
+std::atomic<int> g_inject_stall{0};
+std::atomic<long long> g_wait_limit_ns{0};
 
+constexpr long long kDefaultWaitLimitNs = 2000000000LL;   // 2 s per mbarrier wait
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<unsigned int*> g_status_addr[kMaxDevices];
+
+enum Kind : int { kAuto = 0, kRows = 1, kStream = 2 };
 
 frn_status fail(frn_status s, const char* fmt, ...) {
     va_list ap;
@@ -60,9 +67,33 @@ frn_status sm_count(int* out) {
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Launch shape.  A row's ntiles warp tiles go to C CTAs of a cluster.  The
-// results do not depend on this choice (the reduction tree is fixed by H).
-frn::Plan choose_plan(long long T, int H, int num_sms) {
+}  // namespace
+
+// Device status word of the stream kernel's bounded waits (one per device).
+__device__ unsigned int g_frn_status_word;
+
+namespace {
+
+frn_status status_word(unsigned int** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < kMaxDevices) {
+        unsigned int* a = g_status_addr[dev].load(std::memory_order_acquire);
+        if (a) { *out = a; return FRN_OK; }
+    }
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_frn_status_word);
+    if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < kMaxDevices) g_status_addr[dev].store(static_cast<unsigned int*>(a), std::memory_order_release);
+    *out = static_cast<unsigned int*>(a);
+    return FRN_OK;
+}
+
+// Launch shape of the row kernel.  A row's ntiles warp tiles go to C CTAs of
+// a cluster.  The results do not depend on this choice (the reduction tree is
+// fixed by H).
+frn::RowPlan choose_rows(long long T, int H, int num_sms) {
     const int nvec = H / frn::kVecElems;
     const int ntiles = ceil_div(nvec, frn::kTileVecs);
     const int cmin = ceil_div(ntiles, frn::kMaxTilesPerCta);
@@ -79,12 +110,38 @@ frn::Plan choose_plan(long long T, int H, int num_sms) {
     }
     const int tpc = ceil_div(ntiles, C);
     C = ceil_div(ntiles, tpc);   // no empty CTA
-    frn::Plan plan;
+    frn::RowPlan plan;
     plan.ctas_per_row = C;
     plan.tiles_per_cta = tpc;
     plan.threads = tpc * 32;
     plan.grid = T * C;
     return plan;
+}
+
+// Launch shape of the stream kernel: at most 16 consumer warps with 1, 2 or 4
+// tiles each, as many row-slice slots as fit in 227 KB, one CTA per SM.
+frn::StreamPlan choose_stream(long long T, int H, int num_sms) {
+    const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
+    int tpw = ceil_div(ntiles, frn::kStreamMaxConsumerWarps);
+    tpw = tpw <= 1 ? 1 : (tpw <= 2 ? 2 : 4);
+    frn::StreamPlan plan;
+    plan.tiles_per_warp = tpw;
+    plan.consumer_warps = ceil_div(ntiles, tpw);
+    const int slice = 2 * H;
+    int slots = (frn::kStreamSmemLimit - frn::kStreamSmemReserve) / slice;
+    if (slots > frn::kStreamMaxSlots) slots = frn::kStreamMaxSlots;
+    plan.slots = slots;
+    plan.smem_bytes = frn::stream_smem_bytes(slots, slice);
+    plan.grid = T < num_sms ? T : num_sms;
+    return plan;
+}
+
+// Which kernel: the row kernel while the rows alone cannot keep every SM
+// streaming, the stream kernel beyond.
+int choose_kind(long long T, int num_sms) {
+    const int forced = g_force_kernel.load(std::memory_order_relaxed);
+    if (forced == kRows || forced == kStream) return forced;
+    return T >= 2LL * num_sms ? kStream : kRows;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -101,106 +158,221 @@ Range range_of(const void* p, long long bytes, const char* name) {
     return Range{lo, lo + static_cast<uintptr_t>(bytes), name};
 }
 
-// Shared by both entry points.  quant: 0 = none, 1 = variant A (y NULL),
-// 2 = variant B.
-frn_status run(const void* const* partials, int R, const void* residual, const void* gamma,
-               void* residual_out, void* y, void* q, float* scales, int64_t T, int H,
-               float eps, int group_size, int quant, frn_stream_t stream) {
-    // ---- scalar arguments
+// One call's arguments.  quant: 0 = none, 1 = variant A (no bf16 y output),
+// 2 = variant B.  The workspace fields are used by the unfused paths only.
+struct Call {
+    const void* const* partials;
+    int R;
+    const void* residual;
+    const void* gamma;
+    void* residual_out;
+    void* y;
+    void* q;
+    float* scales;
+    int64_t T;
+    int H;
+    float eps;
+    int group_size;
+    int quant;
+    void* workspace;
+    long long workspace_bytes;
+    long long workspace_needed;
+};
+
+// Everything that can be checked on the host: scalars, pointers, alignment,
+// overlap.  Returns FRN_OK with *empty set when T == 0 (nothing to launch).
+frn_status validate(const Call& c, bool* empty) {
+    *empty = false;
+    const int R = c.R, H = c.H;
+    const int64_t T = c.T;
     if (R < 1) return fail(FRN_ERR_INVALID_ARG, "R=%d must be >= 1", R);
     if (R > FRN_MAX_PARTIALS) return fail(FRN_ERR_UNSUPPORTED, "R=%d exceeds %d", R, FRN_MAX_PARTIALS);
     if (T < 0) return fail(FRN_ERR_INVALID_ARG, "T=%lld must be >= 0", static_cast<long long>(T));
     if (H < 1) return fail(FRN_ERR_INVALID_ARG, "H=%d must be >= 1", H);
     if (H % 8 != 0 || H > FRN_MAX_HIDDEN)
         return fail(FRN_ERR_UNSUPPORTED, "H=%d must be a multiple of 8 and <= %d", H, FRN_MAX_HIDDEN);
-    if (!std::isfinite(eps) || eps < 0.0f) return fail(FRN_ERR_INVALID_ARG, "eps must be finite and >= 0");
-    if (quant) {
-        if (group_size < 1 || H % group_size != 0)
-            return fail(FRN_ERR_INVALID_ARG, "group_size=%d must divide H=%d", group_size, H);
-        if (group_size != FRN_QUANT_GROUP)
-            return fail(FRN_ERR_UNSUPPORTED, "group_size=%d: only %d is built", group_size, FRN_QUANT_GROUP);
+    if (!std::isfinite(c.eps) || c.eps < 0.0f) return fail(FRN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (c.quant) {
+        if (c.group_size < 1 || H % c.group_size != 0)
+            return fail(FRN_ERR_INVALID_ARG, "group_size=%d must divide H=%d", c.group_size, H);
+        if (c.group_size != FRN_QUANT_GROUP)
+            return fail(FRN_ERR_UNSUPPORTED, "group_size=%d: only %d is built", c.group_size, FRN_QUANT_GROUP);
     }
     // Nothing to do (and zero-size buffers may legitimately be NULL).
-    if (T == 0) return ok();
-    // ---- pointers
-    if (!partials) return fail(FRN_ERR_INVALID_ARG, "partials array is NULL");
+    if (T == 0) {
+        *empty = true;
+        return ok();
+    }
+    if (!c.partials) return fail(FRN_ERR_INVALID_ARG, "partials array is NULL");
     for (int r = 0; r < R; ++r) {
-        if (!partials[r]) return fail(FRN_ERR_INVALID_ARG, "partials[%d] is NULL", r);
-        if (!aligned(partials[r], 16)) return fail(FRN_ERR_MISALIGNED, "partials[%d] not 16-byte aligned", r);
+        if (!c.partials[r]) return fail(FRN_ERR_INVALID_ARG, "partials[%d] is NULL", r);
+        if (!aligned(c.partials[r], 16)) return fail(FRN_ERR_MISALIGNED, "partials[%d] not 16-byte aligned", r);
     }
-    if (!gamma) return fail(FRN_ERR_INVALID_ARG, "gamma is NULL");
-    if (!residual_out) return fail(FRN_ERR_INVALID_ARG, "residual_out is NULL");
-    if (quant != 1 && !y) return fail(FRN_ERR_INVALID_ARG, "y is NULL");
-    if (quant && (!q || !scales)) return fail(FRN_ERR_INVALID_ARG, "q / scales is NULL");
-    if (!aligned(gamma, 16)) return fail(FRN_ERR_MISALIGNED, "gamma not 16-byte aligned");
-    if (residual && !aligned(residual, 16)) return fail(FRN_ERR_MISALIGNED, "residual not 16-byte aligned");
-    if (!aligned(residual_out, 16)) return fail(FRN_ERR_MISALIGNED, "residual_out not 16-byte aligned");
-    if (y && !aligned(y, 16)) return fail(FRN_ERR_MISALIGNED, "y not 16-byte aligned");
-    if (quant && !aligned(q, 16)) return fail(FRN_ERR_MISALIGNED, "q not 16-byte aligned");
-    if (quant && !aligned(scales, 4)) return fail(FRN_ERR_MISALIGNED, "scales not 4-byte aligned");
-    // T * H bf16 elements must be addressable and the grid must fit.
+    if (!c.gamma) return fail(FRN_ERR_INVALID_ARG, "gamma is NULL");
+    if (!c.residual_out) return fail(FRN_ERR_INVALID_ARG, "residual_out is NULL");
+    if (c.quant != 1 && !c.y) return fail(FRN_ERR_INVALID_ARG, "y is NULL");
+    if (c.quant && (!c.q || !c.scales)) return fail(FRN_ERR_INVALID_ARG, "q / scales is NULL");
+    if (!aligned(c.gamma, 16)) return fail(FRN_ERR_MISALIGNED, "gamma not 16-byte aligned");
+    if (c.residual && !aligned(c.residual, 16)) return fail(FRN_ERR_MISALIGNED, "residual not 16-byte aligned");
+    if (!aligned(c.residual_out, 16)) return fail(FRN_ERR_MISALIGNED, "residual_out not 16-byte aligned");
+    if (c.y && !aligned(c.y, 16)) return fail(FRN_ERR_MISALIGNED, "y not 16-byte aligned");
+    if (c.quant && !aligned(c.q, 16)) return fail(FRN_ERR_MISALIGNED, "q not 16-byte aligned");
+    if (c.quant && !aligned(c.scales, 4)) return fail(FRN_ERR_MISALIGNED, "scales not 4-byte aligned");
     if (T > (1LL << 40) / H) return fail(FRN_ERR_UNSUPPORTED, "T*H too large");
-
-    // ---- overlap: outputs pairwise disjoint and disjoint from inputs, except
-    // residual_out == residual (in place).
-    const long long act = 2LL * T * H;
-    Range outs[4];
-    int nout = 0;
-    outs[nout++] = range_of(residual_out, act, "residual_out");
-    if (y) outs[nout++] = range_of(y, act, "y");
-    if (quant) {
-        outs[nout++] = range_of(q, T * static_cast<long long>(H), "q");
-        outs[nout++] = range_of(scales, 4LL * T * (H / group_size), "scales");
+    if (c.workspace_needed > 0) {
+        if (!c.workspace) return fail(FRN_ERR_INVALID_ARG, "workspace is NULL (%lld bytes needed)", c.workspace_needed);
+        if (!aligned(c.workspace, 16)) return fail(FRN_ERR_MISALIGNED, "workspace not 16-byte aligned");
+        if (c.workspace_bytes < c.workspace_needed)
+            return fail(FRN_ERR_INVALID_ARG, "workspace has %lld bytes, %lld needed", c.workspace_bytes,
+                        c.workspace_needed);
     }
+
+    // Outputs (and the workspace) pairwise disjoint and disjoint from inputs,
+    // except residual_out == residual (in place).
+    const long long act = 2LL * T * H;
+    Range outs[5];
+    int nout = 0;
+    outs[nout++] = range_of(c.residual_out, act, "residual_out");
+    if (c.y) outs[nout++] = range_of(c.y, act, "y");
+    if (c.quant) {
+        outs[nout++] = range_of(c.q, T * static_cast<long long>(H), "q");
+        outs[nout++] = range_of(c.scales, 4LL * T * (H / c.group_size), "scales");
+    }
+    if (c.workspace_needed > 0) outs[nout++] = range_of(c.workspace, c.workspace_needed, "workspace");
     for (int a = 0; a < nout; ++a)
         for (int b = a + 1; b < nout; ++b)
             if (overlap(outs[a], outs[b]))
-                return fail(FRN_ERR_INVALID_ARG, "outputs %s and %s overlap", outs[a].name, outs[b].name);
+                return fail(FRN_ERR_INVALID_ARG, "%s and %s overlap", outs[a].name, outs[b].name);
     for (int a = 0; a < nout; ++a) {
         for (int r = 0; r < R; ++r)
-            if (overlap(outs[a], range_of(partials[r], act, "partial")))
-                return fail(FRN_ERR_INVALID_ARG, "output %s overlaps partials[%d]", outs[a].name, r);
-        if (overlap(outs[a], range_of(gamma, 2LL * H, "gamma")))
-            return fail(FRN_ERR_INVALID_ARG, "output %s overlaps gamma", outs[a].name);
-        if (residual && overlap(outs[a], range_of(residual, act, "residual"))) {
-            const bool in_place = (a == 0) && residual_out == residual;
-            if (!in_place) return fail(FRN_ERR_INVALID_ARG, "output %s overlaps residual", outs[a].name);
+            if (overlap(outs[a], range_of(c.partials[r], act, "partial")))
+                return fail(FRN_ERR_INVALID_ARG, "%s overlaps partials[%d]", outs[a].name, r);
+        if (overlap(outs[a], range_of(c.gamma, 2LL * H, "gamma")))
+            return fail(FRN_ERR_INVALID_ARG, "%s overlaps gamma", outs[a].name);
+        if (c.residual && overlap(outs[a], range_of(c.residual, act, "residual"))) {
+            const bool in_place = (a == 0) && c.residual_out == c.residual;
+            if (!in_place) return fail(FRN_ERR_INVALID_ARG, "%s overlaps residual", outs[a].name);
         }
     }
+    return ok();
+}
 
-    int sms = 0;
-    frn_status st = sm_count(&sms);
-    if (st != FRN_OK) return st;
-    const frn::Plan plan = choose_plan(T, H, sms);
-    if (plan.grid > 0x7FFFFFFFLL) return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(T));
-
+frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::StreamPlan& splan,
+                        unsigned int* status) {
     frn::Params p;
     std::memset(&p, 0, sizeof(p));
     for (int r = 0; r < frn::kMaxPartials; ++r)
-        p.partials[r] = static_cast<const uint4*>(partials[r < R ? r : 0]);
-    p.residual = static_cast<const uint4*>(residual);
-    p.gamma = static_cast<const uint4*>(gamma);
-    p.residual_out = static_cast<uint4*>(residual_out);
-    p.y = static_cast<uint4*>(y);
-    p.q = static_cast<uint2*>(q);
-    p.scales = scales;
-    p.T = T;
-    p.R = R;
-    p.H = H;
-    p.nvec = H / frn::kVecElems;
+        p.partials[r] = static_cast<const uint4*>(c.partials[r < c.R ? r : 0]);
+    p.residual = static_cast<const uint4*>(c.residual);
+    p.gamma = static_cast<const uint4*>(c.gamma);
+    p.residual_out = static_cast<uint4*>(c.residual_out);
+    p.y = static_cast<uint4*>(c.y);
+    p.q = static_cast<uint2*>(c.q);
+    p.scales = c.scales;
+    p.T = c.T;
+    p.R = c.R;
+    p.H = c.H;
+    p.nvec = c.H / frn::kVecElems;
     p.ntiles = ceil_div(p.nvec, frn::kTileVecs);
-    p.tiles_per_cta = plan.tiles_per_cta;
-    p.ctas_per_row = plan.ctas_per_row;
-    p.eps = eps;
+    p.tiles_per_cta = rplan.tiles_per_cta;
+    p.ctas_per_row = rplan.ctas_per_row;
+    p.eps = c.eps;
+    p.nslices = c.R + (c.residual ? 1 : 0);
+    p.consumer_warps = splan.consumer_warps;
+    p.slots = splan.slots;
+    p.slice_bytes = 2 * c.H;
+    const long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.wait_limit_ns = static_cast<unsigned long long>(lim > 0 ? lim : kDefaultWaitLimitNs);
+    p.inject_stall = g_inject_stall.load(std::memory_order_relaxed);
+    p.error_word = status;
+    return p;
+}
 
+// The fused epilogue (one kernel).  quant as in Call; the kernel writes c.y
+// when it is not NULL.
+frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
+    const int kind = choose_kind(c.T, sms);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, sms);
+    const frn::StreamPlan splan = choose_stream(c.T, c.H, sms);
+    if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
+        return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
+    unsigned int* status = nullptr;
+    if (kind == kStream) {
+        frn_status st = status_word(&status);
+        if (st != FRN_OK) return st;
+    }
+    const frn::Params p = make_params(c, rplan, splan, status);
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    switch (quant) {
-        case 0: e = frn::launch_norm(p, plan, s, pdl); break;
-        case 1: e = frn::launch_quant_a(p, plan, s, pdl); break;
-        default: e = frn::launch_quant_b(p, plan, s, pdl); break;
+    if (kind == kStream) {
+        switch (quant) {
+            case 0: e = frn::launch_stream_norm(p, splan, s, pdl); break;
+            case 1: e = frn::launch_stream_quant_a(p, splan, s, pdl); break;
+            default: e = frn::launch_stream_quant_b(p, splan, s, pdl); break;
+        }
+    } else {
+        switch (quant) {
+            case 0: e = frn::launch_rows_norm(p, rplan, s, pdl); break;
+            case 1: e = frn::launch_rows_quant_a(p, rplan, s, pdl); break;
+            default: e = frn::launch_rows_quant_b(p, rplan, s, pdl); break;
+        }
     }
+    if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+frn_status run(const Call& c, frn_stream_t stream) {
+    bool empty = false;
+    frn_status st = validate(c, &empty);
+    if (st != FRN_OK || empty) return st;
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != FRN_OK) return st;
+    return launch_fused(c, c.quant, sms, stream);
+}
+
+// ---------------------------------------------------------- unfused paths --
+
+long long unfused_workspace(int64_t T, int H, int stages, bool quant, bool emit_y) {
+    if (T <= 0 || H <= 0) return 0;
+    long long b = 0;
+    if (stages == 3 || !quant) b += 4LL * T * H;   // fp32 sum of the partials
+    if (quant && !emit_y) b += 2LL * T * H;        // bf16 y between norm and quant
+    return b;
+}
+
+frn_status run_unfused(Call c, int stages, frn_stream_t stream) {
+    if (!(stages == 2 || (stages == 3 && c.quant)))
+        return fail(FRN_ERR_INVALID_ARG, "stages=%d: 2, or 3 with quant", stages);
+    c.workspace_needed = unfused_workspace(c.T, c.H, stages, c.quant != 0, c.y != nullptr);
+    bool empty = false;
+    frn_status st = validate(c, &empty);
+    if (st != FRN_OK || empty) return st;
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != FRN_OK) return st;
+    const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(c.workspace);
+    const bool need_x = stages == 3 || !c.quant;
+    float4* xsum = need_x ? reinterpret_cast<float4*>(ws) : nullptr;
+    uint4* ytarget = c.y ? static_cast<uint4*>(c.y)
+                         : reinterpret_cast<uint4*>(ws + (need_x ? 4LL * c.T * c.H : 0));
+    Call norm = c;
+    norm.y = ytarget;
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, sms);
+    const frn::StreamPlan splan = choose_stream(c.T, c.H, sms);
+    frn::Params p = make_params(norm, rplan, splan, nullptr);
+    cudaError_t e = cudaSuccess;
+    if (need_x) {
+        e = frn::launch_reduce(p, xsum, sms, s, pdl);
+        if (e == cudaSuccess) e = frn::launch_addnorm(p, xsum, ytarget, s, pdl);
+    } else {
+        st = launch_fused(norm, 0, sms, stream);
+        if (st != FRN_OK) return st;
+    }
+    if (e == cudaSuccess && c.quant) e = frn::launch_quant(p, ytarget, sms, s, pdl);
     if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -210,8 +382,9 @@ frn_status run(const void* const* partials, int R, const void* residual, const v
 FRN_EXPORT frn_status fused_reduce_rmsnorm(const void* const* partials, int R, const void* residual,
                                            const void* gamma, void* residual_out, void* y, int64_t T,
                                            int H, float eps, frn_stream_t stream) {
-    return run(partials, R, residual, gamma, residual_out, y, nullptr, nullptr, T, H, eps,
-               FRN_QUANT_GROUP, 0, stream);
+    const Call c{partials, R, residual, gamma, residual_out, y, nullptr, nullptr, T, H, eps, FRN_QUANT_GROUP,
+                 0, nullptr, 0, 0};
+    return run(c, stream);
 }
 
 FRN_EXPORT frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* partials, int R,
@@ -219,8 +392,25 @@ FRN_EXPORT frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* pa
                                                            void* residual_out, void* y, void* q_e4m3,
                                                            float* scales, int64_t T, int H, float eps,
                                                            int group_size, frn_stream_t stream) {
-    return run(partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps, group_size,
-               y ? 2 : 1, stream);
+    const Call c{partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps, group_size,
+                 y ? 2 : 1, nullptr, 0, 0};
+    return run(c, stream);
+}
+
+FRN_EXPORT int64_t frn_unfused_workspace_bytes(int64_t T, int H, int stages, int quant, int emit_y) {
+    if (!(stages == 2 || (stages == 3 && quant))) return -1;
+    return unfused_workspace(T, H, stages, quant != 0, emit_y != 0);
+}
+
+FRN_EXPORT frn_status frn_unfused_reduce_rmsnorm(const void* const* partials, int R, const void* residual,
+                                                 const void* gamma, void* residual_out, void* y, void* q_e4m3,
+                                                 float* scales, int64_t T, int H, float eps, int group_size,
+                                                 int stages, void* workspace, int64_t workspace_bytes,
+                                                 frn_stream_t stream) {
+    const int quant = q_e4m3 || scales ? (y ? 2 : 1) : 0;
+    const Call c{partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps,
+                 quant ? group_size : FRN_QUANT_GROUP, quant, workspace, workspace_bytes, 0};
+    return run_unfused(c, stages, stream);
 }
 
 FRN_EXPORT const char* frn_status_string(frn_status s) {
@@ -251,7 +441,35 @@ FRN_EXPORT frn_status frn_set_ctas_per_row(int ctas_per_row) {
     return ok();
 }
 
-FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* ctas_per_row,
+FRN_EXPORT frn_status frn_set_kernel(int kernel) {
+    if (kernel < 0 || kernel > 2) return fail(FRN_ERR_INVALID_ARG, "kernel=%d must be 0, 1 or 2", kernel);
+    g_force_kernel.store(kernel, std::memory_order_relaxed);
+    return ok();
+}
+
+FRN_EXPORT frn_status frn_set_test_hooks(int inject_stall, int64_t wait_limit_ns) {
+    g_inject_stall.store(inject_stall ? 1 : 0, std::memory_order_relaxed);
+    g_wait_limit_ns.store(wait_limit_ns > 0 ? static_cast<long long>(wait_limit_ns) : 0, std::memory_order_relaxed);
+    return ok();
+}
+
+FRN_EXPORT frn_status frn_device_status(int clear) {
+    unsigned int* addr = nullptr;
+    frn_status st = status_word(&addr);
+    if (st != FRN_OK) return st;
+    unsigned int word = 0;
+    cudaError_t e = cudaMemcpy(&word, addr, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+    if (clear && word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "clearing the status word: %s", cudaGetErrorString(e));
+    }
+    if (word & frn::kErrWaitTimeout) return fail(FRN_ERR_TIMEOUT, "a bounded device-side wait ran out");
+    return ok();
+}
+
+FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int* ctas_per_row,
                                        int* threads_per_cta, int64_t* grid_ctas) {
     (void)quant;
     if (R < 1 || T < 0 || H < 8 || H % 8 != 0 || H > FRN_MAX_HIDDEN)
@@ -259,9 +477,18 @@ FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* 
     int sms = 0;
     frn_status st = sm_count(&sms);
     if (st != FRN_OK) return st;
-    const frn::Plan plan = choose_plan(T, H, sms);
-    if (ctas_per_row) *ctas_per_row = plan.ctas_per_row;
-    if (threads_per_cta) *threads_per_cta = plan.threads;
-    if (grid_ctas) *grid_ctas = plan.grid;
+    const int kind = choose_kind(T, sms);
+    if (kernel) *kernel = kind;
+    if (kind == kStream) {
+        const frn::StreamPlan plan = choose_stream(T, H, sms);
+        if (ctas_per_row) *ctas_per_row = 1;
+        if (threads_per_cta) *threads_per_cta = (plan.consumer_warps + 1) * 32;
+        if (grid_ctas) *grid_ctas = plan.grid;
+    } else {
+        const frn::RowPlan plan = choose_rows(T, H, sms);
+        if (ctas_per_row) *ctas_per_row = plan.ctas_per_row;
+        if (threads_per_cta) *threads_per_cta = plan.threads;
+        if (grid_ctas) *grid_ctas = plan.grid;
+    }
     return ok();
 }

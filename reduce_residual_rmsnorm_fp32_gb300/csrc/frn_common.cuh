@@ -1,0 +1,315 @@
+// frn_common.cuh -- shared device code of the fused reduce + residual add +
+// RMSNorm (+ per-group-128 dynamic FP8 e4m3) epilogue for sm_103a: parameter
+// block, PTX wrappers, number formats and the per-vector arithmetic that both
+// kernel families (frn_rows.cuh, frn_stream.cuh) run identically.
+//
+// The op, per token row (include/frn.h has the full contract):
+//   x_hat = sum_r f32(P[r]) (rank order) + f32(residual);  residual_out = bf16(x_hat)
+//   y = bf16((x * rstd) * gamma),  rstd = 1/sqrt(sum(x^2)/H + eps),  x = f32(residual_out)
+//   per 128-group of y: s = max|y| / 448, q = e4m3(y / s)
+// following the replaced subgraph all_reduce -> (fused_add_)rms_norm of the
+// "ROCm AITER fused all-reduce + RMSNorm" page (vLLM PR 37646 summary, key source
+// snippets) and the per-1x128 quant of the normalised bf16 activation of the
+// "AMD fused AllReduce-RMSNorm quant kernel" page (SGLang PR 24651 summary).
+//
+// Work decomposition shared by both kernels:
+//  * A row of H bf16 is split into 16-byte vectors of 8 elements (nvec = H/8) and
+//    the vectors into "tiles" of 32; lane l of the warp owning tile k holds
+//    vector 32*k + l.  A quant group (128 elements) is an aligned half-warp.
+//  * Sum of squares: a fixed tree whose shape depends on H alone -- an fp32 FMA
+//    chain over the 8 elements of a vector, a 32-lane xor butterfly within the
+//    tile, then tile slots k and k+32 paired and a second butterfly over the 32
+//    pairs (absent tiles are +0).  Every lane ends with the same bits, and a row
+//    gives the same bits whichever kernel, launch shape or T computes it.
+//  * Ordering: griddepcontrol.wait precedes every global access, so with
+//    programmatic dependent launch the prologue overlaps the previous kernel but
+//    no partial is read before its producer has completed (the lesson of the
+//    missing end_sync barrier in "Fix: add missing end_sync barrier in fused
+//    allreduce+rmsnorm kernel", AITER PR 4346).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace frn {
+
+constexpr int kMaxPartials = 16;
+constexpr int kVecElems = 8;        // bf16 per 16-byte vector
+constexpr int kTileVecs = 32;       // vectors per warp tile
+constexpr int kMaxTilesPerCta = 16; // 512 threads
+constexpr int kMaxTiles = 64;       // H <= 16384 (two tile slots per lane)
+constexpr int kMaxThreads = kMaxTilesPerCta * 32;
+constexpr int kGroup = 128;         // quant group (elements)
+
+enum Mode : int { kNorm = 0, kQuantA = 1, kQuantB = 2 };
+
+struct Params {
+    const uint4* partials[kMaxPartials];
+    const uint4* residual;   // nullptr: zeros
+    const uint4* gamma;
+    uint4* residual_out;
+    uint4* y;                // bf16 output (kNorm, kQuantB)
+    uint2* q;                // e4m3 codes, 8 per vector (kQuantA, kQuantB)
+    float* scales;           // [T, H/128]
+    long long T;
+    int R;
+    int H;
+    int nvec;                // H / 8
+    int ntiles;              // ceil(nvec / 32)
+    int tiles_per_cta;       // warps per CTA
+    int ctas_per_row;        // cluster size (row kernel)
+    float eps;
+    // stream kernel
+    int nslices;             // bulk copies per row: R partials, then the residual if any
+    int consumer_warps;
+    int slots;               // shared-memory ring slots, one row slice (2*H bytes) each
+    int slice_bytes;
+    unsigned long long wait_limit_ns;   // bound on every mbarrier wait
+    int inject_stall;        // test hook: never issue the first copy (forces a timeout)
+    unsigned int* error_word;           // device status word, set on a timed-out wait
+};
+
+// Bits of the device status word.
+constexpr unsigned kErrWaitTimeout = 1u;
+
+// ------------------------------------------------------------------ PTX ----
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Streaming 128-bit load of data that is read once: non-coherent read-only
+// path, no L1 allocation, 256-byte L2 sector prefetch.  Predicated inside the
+// asm so that no branch is generated; a disabled load yields zeros.
+__device__ __forceinline__ uint4 ld_stream(const uint4* ptr, bool pred) {
+    uint4 v;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@p ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "r"((int)pred));
+    return v;
+}
+
+// Coherent 128-bit load, for the residual (which residual_out may overwrite in
+// place) -- same hints otherwise.
+__device__ __forceinline__ uint4 ld_coherent(const uint4* ptr, bool pred) {
+    uint4 v;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@p ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "r"((int)pred));
+    return v;
+}
+
+// gamma is re-read by every row: keep it cacheable.
+__device__ __forceinline__ uint4 ld_keep(const uint4* ptr, bool pred) {
+    uint4 v;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@p ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "r"((int)pred));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a float from the shared memory of CTA `rank` of this cluster, at the
+// address that `local` has in this CTA's shared window.
+__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ------------------------------------------------------- number formats ----
+
+// bf16 pair in one 32-bit word: element 2i in the low half, 2i+1 in the high half.
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// cvt.rn.bf16x2.f32 d, a, b puts bf16(a) in the upper half and bf16(b) in the lower.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    return v;
+}
+
+// OCP e4m3 ("fn"), round to nearest even, saturating to +-448; the upper byte
+// of the result holds the first source operand.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4 v) {
+    float f[8];
+    unpack8(v, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+}
+
+__device__ __forceinline__ float butterfly_sum(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+    return v;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------- mbarrier + bulk copy ----
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// 1-D bulk copy global -> shared (TMA, non-tensor form), completing `bytes`
+// transaction bytes on the mbarrier.  Both addresses 16-byte aligned, size a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// ------------------------------------------------- per-vector arithmetic ----
+
+// Sum of squares of one tile: x <- f32(ro); FMA chain over the 8 elements of
+// this lane's vector; xor butterfly over the 32 lanes.
+__device__ __forceinline__ float tile_sumsq(const uint4 ro, float (&x)[8]) {
+    unpack8(ro, x);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s = __fmaf_rn(x[i], x[i], s);
+    return butterfly_sum(s);
+}
+
+// rstd from the row's tile slots `lane` (lo) and `lane + 32` (hi).
+__device__ __forceinline__ float row_rstd(float lo, float hi, int H, float eps) {
+    const float ss = butterfly_sum(__fadd_rn(lo, hi));
+    return __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(H)), eps));
+}
+
+// y = bf16((x * rstd) * gamma) for one vector.
+__device__ __forceinline__ uint4 rms_y(const float (&x)[8], float rstd, const uint4 g) {
+    float gf[8], yv[8];
+    unpack8(g, gf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(__fmul_rn(x[i], rstd), gf[i]);
+    return pack8(yv);
+}
+
+// Per-group dynamic e4m3 of one bf16 y vector.  All 32 lanes must call it (the
+// group absmax is a half-warp shuffle).  s = absmax / 448; q = e4m3(y / s),
+// q = 0 when s == 0.
+__device__ __forceinline__ void quant8(const uint4 yb, uint2& qq, float& sc) {
+    float yq[8];
+    unpack8(yb, yq);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(yq[i]));
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    sc = __fdiv_rn(amax, 448.0f);
+    qq = make_uint2(0u, 0u);
+    if (sc != 0.0f) {
+        float qv[8];
+        if (sc >= 0x1p-64f) {
+            // y / s, correctly rounded, from one reciprocal per group:
+            // q0 = RN(y * RN(1/s)), then one FMA correction with the residual
+            // y - s*q0 (Markstein's theorem).  Checked exhaustively for every
+            // bf16 significand of y against every significand s = RN(absmax/448)
+            // can take; powers of two scale these exactly in this range.
+            const float rs = __frcp_rn(sc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float q0 = __fmul_rn(yq[i], rs);
+                const float rem = __fmaf_rn(-sc, q0, yq[i]);
+                qv[i] = __fmaf_rn(rem, rs, q0);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qv[i] = __fdiv_rn(yq[i], sc);
+        }
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = pack_e4m3x2(qv[2 * i], qv[2 * i + 1]);
+        qq.x = c[0] | (c[1] << 16);
+        qq.y = c[2] | (c[3] << 16);
+    }
+}
+
+}  // namespace frn

@@ -1,0 +1,150 @@
+// frn_rows.cuh -- the row kernel: one token row per thread-block cluster.
+//
+// The tiles of a row are spread over C CTAs of one cluster (tiles_per_cta
+// warps each, one tile per warp).  For decode-sized T this puts one row on up
+// to 8 SMs, so a handful of tokens still engages most of the GPU.  Every thread
+// issues all of its R+1 128-bit loads (partials through the read-only path, no
+// L1 allocation, 256-byte L2 prefetch) before its first add, so each byte of
+// HBM is read exactly once and the row stays in registers until y is written.
+// Tile sums cross CTAs through distributed shared memory after one cluster
+// barrier; a second (split) barrier keeps each CTA's shared memory alive until
+// its peers have read it.
+#pragma once
+
+#include "frn_common.cuh"
+
+namespace frn {
+
+// RMAX is the unrolled partial count (R <= RMAX; loads beyond R are predicated
+// off).  CLUSTER == false is the single-CTA row (no cluster barriers).
+template <int RMAX, int MODE, bool CLUSTER>
+__global__ void __launch_bounds__(kMaxThreads) frn_row_kernel(const __grid_constant__ Params p) {
+    __shared__ float tile_sum[kMaxTilesPerCta];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int rank = 0;
+    long long row;
+    if constexpr (CLUSTER) {
+        rank = static_cast<int>(cluster_ctarank());
+        row = blockIdx.x / p.ctas_per_row;
+    } else {
+        row = blockIdx.x;
+    }
+    const int tile = rank * p.tiles_per_cta + warp;
+    const int j = tile * kTileVecs + lane;              // vector index in the row
+    const bool valid = j < p.nvec;
+    const long long off = row * static_cast<long long>(p.nvec) + j;
+
+    // Nothing of the previous kernel on the stream may be read (or overwritten)
+    // before it has completed.
+    grid_dependency_wait();
+
+    uint4 raw[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) raw[r] = ld_stream(p.partials[r] + off, valid && r < p.R);
+    const uint4 res = ld_coherent(p.residual + off, valid && p.residual != nullptr);
+    const uint4 g = ld_keep(p.gamma + j, valid);
+    launch_dependents();
+
+    // fp32 sum in rank order, residual last (+0 when absent), one RNE to bf16.
+    float acc[8];
+    unpack8(raw[0], acc);
+#pragma unroll
+    for (int r = 1; r < RMAX; ++r)
+        if (r < p.R) add8(acc, raw[r]);
+    add8(acc, res);
+    const uint4 ro = pack8(acc);
+    if (valid) p.residual_out[off] = ro;
+
+    float x[8];
+    const float s = tile_sumsq(ro, x);
+    if (lane == 0) tile_sum[warp] = s;
+    __syncwarp();
+
+    float lo, hi;   // tile slots `lane` and `lane + 32` of the row
+    if constexpr (CLUSTER) {
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        const int tpc = p.tiles_per_cta;
+        lo = lane < p.ntiles ? ld_dsmem(&tile_sum[lane % tpc], lane / tpc) : 0.0f;
+        hi = lane + 32 < p.ntiles ? ld_dsmem(&tile_sum[(lane + 32) % tpc], (lane + 32) / tpc) : 0.0f;
+        __syncwarp();
+        // Done reading the other CTAs' shared memory; they may exit once all
+        // CTAs have arrived here (matching wait at the end).
+        cluster_arrive_release();
+    } else {
+        __syncthreads();
+        lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
+        hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
+    }
+    const float rstd = row_rstd(lo, hi, p.H, p.eps);
+    const uint4 yb = rms_y(x, rstd, g);
+    if constexpr (MODE != kQuantA) {
+        if (valid) p.y[off] = yb;
+    }
+    if constexpr (MODE != kNorm) {
+        uint2 qq;
+        float sc;
+        quant8(yb, qq, sc);
+        if (valid) {
+            p.q[off] = qq;
+            if ((lane & 15) == 0) p.scales[row * (p.H / kGroup) + (j >> 4)] = sc;
+        }
+    }
+
+    if constexpr (CLUSTER) {
+        __syncwarp();
+        cluster_wait_acquire();
+    }
+}
+
+struct RowPlan {
+    int ctas_per_row;
+    int tiles_per_cta;
+    int threads;
+    long long grid;
+};
+
+template <int RMAX, int MODE, bool CLUSTER>
+cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    unsigned n = 0;
+    if constexpr (CLUSTER) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = static_cast<unsigned>(plan.ctas_per_row);
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, frn_row_kernel<RMAX, MODE, CLUSTER>, p);
+}
+
+// Dispatch on the unrolled partial count and on whether the row spans a cluster.
+template <int MODE>
+cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
+    const bool cl = plan.ctas_per_row > 1;
+#define FRN_DISPATCH_R(RM)                                                        \
+    return cl ? launch_row_one<RM, MODE, true>(p, plan, stream, pdl)             \
+              : launch_row_one<RM, MODE, false>(p, plan, stream, pdl)
+    if (p.R <= 1) FRN_DISPATCH_R(1);
+    if (p.R <= 2) FRN_DISPATCH_R(2);
+    if (p.R <= 4) FRN_DISPATCH_R(4);
+    if (p.R <= 8) FRN_DISPATCH_R(8);
+    FRN_DISPATCH_R(16);
+#undef FRN_DISPATCH_R
+}
+
+}  // namespace frn

@@ -1,0 +1,267 @@
+// frn_stream.cuh -- the stream kernel: persistent, warp-specialised, for many
+// token rows.
+//
+// One CTA per SM walks rows blockIdx.x, blockIdx.x + gridDim.x, ...  A row is
+// read as nslices contiguous slices of 2*H bytes (the R partials, then the
+// residual), and each slice is one 1-D bulk copy (TMA, cp.async.bulk) into a
+// ring of shared-memory slots:
+//  * producer warp, one lane: wait until a slot is empty, arm its "full"
+//    mbarrier with the slice's byte count, issue the bulk copy;
+//  * consumer warps (one or more tiles each): wait until the slot is full,
+//    accumulate their vectors from shared memory in slice order (rank order,
+//    residual last), release the slot; after the last slice, run the same
+//    per-vector epilogue as the row kernel (bf16 residual_out, fixed-tree sum
+//    of squares, y, quant), with the tile sums exchanged through shared memory
+//    and one named barrier per row.
+// The ring holds ~220 KB, so up to that many bytes per SM stay in flight while
+// the consumers reduce, normalise and store -- independent of registers.
+//
+// Every mbarrier wait is bounded (wait_limit_ns, from %globaltimer).  A wait
+// that runs out sets kErrWaitTimeout in the device status word and raises a
+// CTA-wide abort flag; all waits then give up, the consumers leave together at
+// the next per-row barrier (an OR-reduction, so the decision is uniform), and
+// the producer waits -- again bounded -- for every bulk copy it issued before
+// the CTA exits.
+#pragma once
+
+#include "frn_common.cuh"
+
+namespace frn {
+
+constexpr int kStreamMaxConsumerWarps = 16;
+constexpr int kStreamThreads = (kStreamMaxConsumerWarps + 1) * 32;
+constexpr int kStreamMaxSlots = 32;
+constexpr int kStreamSmemLimit = 232448;     // 227 KB opt-in per CTA on sm_100-class parts
+constexpr int kStreamSmemReserve = 2048;     // barriers, tile sums, flags (<= 16*32 + 512 + 16)
+
+__host__ __device__ constexpr int stream_smem_bytes(int slots, int slice_bytes) {
+    // data ring | full[slots], empty[slots] | tile sums [2][kMaxTiles] | abort flag
+    return slots * slice_bytes + 16 * slots + 2 * kMaxTiles * 4 + 16;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting or
+// when this wait ran out (which starts the abort).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned long long limit_ns, unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            if (err) atomicOr(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+
+// Named barrier 1 over the consumer warps, OR-reducing a predicate.
+__device__ __forceinline__ bool consumers_sync_or(bool pred, int nthreads) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.or.pred pout, 1, %2, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(out) : "r"((uint32_t)pred), "r"(nthreads) : "memory");
+    return out != 0;
+}
+
+template <int TPW, int MODE>
+__global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int NC = p.consumer_warps;
+    const int S = p.slots;
+    const uint32_t slice = static_cast<uint32_t>(p.slice_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slice);
+    float* tsum = reinterpret_cast<float*>(bars + 2 * S);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tsum + 2 * kMaxTiles);
+    const uint32_t data0 = smem_addr(smem);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = full0 + 8u * S;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, static_cast<uint32_t>(NC));
+        }
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    // Nothing of the previous kernel on the stream may be read (or overwritten)
+    // before it has completed.
+    grid_dependency_wait();
+
+    if (warp == NC) {
+        // ------------------------------------------------------- producer --
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t ph = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (long long row = blockIdx.x; ok && row < p.T; row += gridDim.x) {
+                for (int k = 0; k < p.nslices; ++k) {
+                    if (!wait_bounded(empty0 + 8u * slot, ph ^ 1u, abort_flag, p.wait_limit_ns, p.error_word)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint4* src = (k < p.R ? p.partials[k] : p.residual) + row * static_cast<long long>(p.nvec);
+                    const bool skip = p.inject_stall && row == blockIdx.x && k == 0;
+                    if (!skip) {
+                        mbar_arrive_expect_tx(full0 + 8u * slot, slice);
+                        bulk_g2s(data0 + static_cast<uint32_t>(slot) * slice, src, slice, full0 + 8u * slot);
+                        issued |= 1u << slot;
+                        issued_par = (issued_par & ~(1u << slot)) | (ph << slot);
+                    }
+                    if (++slot == S) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            launch_dependents();
+            // Leave no bulk copy in flight into this CTA's shared memory, on the
+            // normal path (where the consumers have waited for them all) as on
+            // an abort (where they may not have).
+            {
+                for (int s = 0; s < S; ++s) {
+                    if (!((issued >> s) & 1u)) continue;
+                    const uint32_t bar = full0 + 8u * s;
+                    const uint32_t par = (issued_par >> s) & 1u;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(bar, par) && globaltimer_ns() - t0 <= p.wait_limit_ns) {
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers --
+    // gamma stays in registers, except with 4 tiles per warp (H > 8192), where
+    // 17 warps leave 96 registers a thread and gamma is re-read (L2) per row.
+    constexpr bool kGammaInRegs = TPW < 4;
+    int jt[TPW];
+    bool vt[TPW];
+    uint4 g[kGammaInRegs ? TPW : 1];
+#pragma unroll
+    for (int t = 0; t < TPW; ++t) {
+        const int tile = warp + t * NC;
+        jt[t] = tile * kTileVecs + lane;
+        vt[t] = jt[t] < p.nvec;
+        if constexpr (kGammaInRegs) g[t] = ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
+    }
+    const int ng = p.H / kGroup;
+    int slot = 0;
+    uint32_t ph = 0;
+    int prow = 0;
+    bool ok = true;
+    for (long long row = blockIdx.x; row < p.T; row += gridDim.x) {
+        float acc[TPW][8];
+        for (int k = 0; k < p.nslices; ++k) {
+            const bool got = ok && wait_bounded(full0 + 8u * slot, ph, abort_flag, p.wait_limit_ns, p.error_word);
+            ok = got;
+            const uint4* src = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(slot) * slice);
+#pragma unroll
+            for (int t = 0; t < TPW; ++t) {
+                const uint4 v = (got && vt[t]) ? src[jt[t]] : make_uint4(0u, 0u, 0u, 0u);
+                if (k == 0) {
+                    unpack8(v, acc[t]);
+                } else {
+                    add8(acc[t], v);
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && got) mbar_arrive(empty0 + 8u * slot);
+            if (++slot == S) {
+                slot = 0;
+                ph ^= 1u;
+            }
+        }
+        if (p.residual == nullptr) {
+#pragma unroll
+            for (int t = 0; t < TPW; ++t) add8(acc[t], make_uint4(0u, 0u, 0u, 0u));   // +0, as the row kernel
+        }
+        const long long rbase = row * static_cast<long long>(p.nvec);
+        uint4 rov[TPW];   // bf16 residual_out, re-widened for y (cheaper than keeping floats)
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+            rov[t] = pack8(acc[t]);
+            if (ok && vt[t]) p.residual_out[rbase + jt[t]] = rov[t];
+            float xs[8];
+            const float s = tile_sumsq(rov[t], xs);
+            if (lane == 0 && warp + t * NC < p.ntiles) tsum[prow * kMaxTiles + warp + t * NC] = s;
+        }
+        if (consumers_sync_or(!ok || *abort_flag != 0, NC * 32)) break;
+        const float lo = lane < p.ntiles ? tsum[prow * kMaxTiles + lane] : 0.0f;
+        const float hi = lane + 32 < p.ntiles ? tsum[prow * kMaxTiles + lane + 32] : 0.0f;
+        const float rstd = row_rstd(lo, hi, p.H, p.eps);
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+            float x[8];
+            unpack8(rov[t], x);
+            const uint4 gt = kGammaInRegs ? g[kGammaInRegs ? t : 0] : ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
+            const uint4 yb = rms_y(x, rstd, gt);
+            if constexpr (MODE != kQuantA) {
+                if (vt[t]) p.y[rbase + jt[t]] = yb;
+            }
+            if constexpr (MODE != kNorm) {
+                uint2 qq;
+                float sc;
+                quant8(yb, qq, sc);
+                if (vt[t]) {
+                    p.q[rbase + jt[t]] = qq;
+                    if ((lane & 15) == 0) p.scales[row * ng + (jt[t] >> 4)] = sc;
+                }
+            }
+        }
+        prow ^= 1;
+    }
+}
+
+struct StreamPlan {
+    int tiles_per_warp;
+    int consumer_warps;
+    int slots;
+    int smem_bytes;
+    long long grid;
+};
+
+template <int TPW, int MODE>
+cudaError_t launch_stream_one(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl) {
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(frn_stream_kernel<TPW, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStreamSmemLimit);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>((plan.consumer_warps + 1) * 32), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, frn_stream_kernel<TPW, MODE>, p);
+}
+
+template <int MODE>
+cudaError_t launch_stream(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl) {
+    switch (plan.tiles_per_warp) {
+        case 1: return launch_stream_one<1, MODE>(p, plan, stream, pdl);
+        case 2: return launch_stream_one<2, MODE>(p, plan, stream, pdl);
+        default: return launch_stream_one<4, MODE>(p, plan, stream, pdl);
+    }
+}
+
+}  // namespace frn

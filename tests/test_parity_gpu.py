@@ -132,30 +132,56 @@ SHAPES = [
 ]
 
 
+@pytest.fixture(params=[frn.KERNEL_ROWS, frn.KERNEL_STREAM], ids=["rows", "stream"])
+def kernel(request):
+    frn.set_kernel(request.param)
+    yield request.param
+    frn.set_kernel(frn.KERNEL_AUTO)
+
+
 @pytest.mark.parametrize("R,T,H", SHAPES)
 @pytest.mark.parametrize("with_residual", [True, False])
-def test_random_shapes_norm(R, T, H, with_residual):
+def test_random_shapes_norm(R, T, H, with_residual, kernel):
     inp = syn.make_inputs(R, T, H, seed=R * 1000 + T + H, with_residual=with_residual)
-    check_norm(inp, f"R={R} T={T} H={H} res={with_residual}")
+    check_norm(inp, f"R={R} T={T} H={H} res={with_residual} kernel={kernel}")
 
 
 @pytest.mark.parametrize("R,T,H", [s for s in SHAPES if s[2] % 128 == 0])
-def test_random_shapes_quant(R, T, H):
+def test_random_shapes_quant(R, T, H, kernel):
     inp = syn.make_inputs(R, T, H, seed=7 + R * 1000 + T + H, partial_std=0.5)
-    check_quant(inp, f"quant R={R} T={T} H={H}")
+    check_quant(inp, f"quant R={R} T={T} H={H} kernel={kernel}")
 
 
-@pytest.mark.parametrize("ctas", [1, 2, 3, 4, 5, 7, 8])
-def test_forced_cluster_split_is_bit_identical(ctas):
-    """Whatever number of CTAs a row is split over, every output has the same bits."""
-    inp = syn.make_inputs(8, 11, 7168, seed=5, partial_std=0.5)
+@pytest.mark.parametrize("msg", [1 << 20, 64 << 20])
+def test_sweep_each_kernel(msg, kernel):
+    T = syn.sweep_tokens(msg)
+    check_norm(syn.config_sweep(msg, seed=3), f"sweep {msg} B kernel={kernel}",
+               sample_rows(T) if T > 600 else None)
+
+
+def test_prefill_each_kernel(kernel):
+    inp = syn.config_prefill(seed=2)
+    check_quant(inp, f"prefill kernel={kernel}", rows=sample_rows(inp.T, 32, seed=kernel))
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 4, 5, 7, 8, "stream"])
+@pytest.mark.parametrize("H", [7168, 4096, 16384])
+def test_every_launch_shape_is_bit_identical(ctas, H):
+    """Whatever number of CTAs a row is split over, and whichever kernel runs, every
+    output has the same bits."""
+    inp = syn.make_inputs(8, 11, H, seed=5, partial_std=0.5)
     d = DevInputs(inp)
-    base = gpu_quant(d, True)
+    frn.set_kernel(frn.KERNEL_ROWS)
     try:
-        frn.set_ctas_per_row(ctas)
+        base = gpu_quant(d, True)
+        if ctas == "stream":
+            frn.set_kernel(frn.KERNEL_STREAM)
+        else:
+            frn.set_ctas_per_row(ctas)
         got = gpu_quant(d, True)
     finally:
         frn.set_ctas_per_row(0)
+        frn.set_kernel(frn.KERNEL_AUTO)
     for a, b in zip(base, got):
         assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
