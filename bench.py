@@ -450,6 +450,42 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------- profile --
+
+PROFILE_CASES = {
+    # name: (R, T, H, mode, outliers, partial_std)
+    "decode64": (8, 64, H, "norm", False, 0.5),
+    "decode8": (8, 8, H, "norm", False, 0.5),
+    "sweep64M": (8, syn.sweep_tokens(64 << 20), H, "norm", False, 0.5),
+    "sweep16M": (8, syn.sweep_tokens(16 << 20), H, "norm", False, 0.5),
+    "prefill_quant_a": (2, 8192, H, "quant_a", True, 1.0),
+    "prefill_quant_b": (2, 8192, H, "quant_b", True, 1.0),
+    "quant_R4_T32": (4, 32, 4096, "quant_b", False, 0.5),
+}
+
+
+def run_profile_case(name: str, iters: int):
+    """Launch one workload `iters` times (after 2 warm-up calls) and nothing else,
+    for ncu.  No timing is reported."""
+    import reduce_residual_rmsnorm_fp32_gb300 as frn
+    R, T, Hh, mode, outlier, std = PROFILE_CASES[name]
+    p, r, g = syn.make_inputs_device(R, T, Hh, seed=4242, partial_std=std, outlier_frac=0.01 if outlier else 0.0)
+    ro = torch.empty((T, Hh), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(ro) if mode != "quant_a" else None
+    q = torch.empty((T, Hh), dtype=torch.float8_e4m3fn, device="cuda") if mode != "norm" else None
+    s = torch.empty((T, Hh // 128), dtype=torch.float32, device="cuda") if mode != "norm" else None
+    for _ in range(2 + iters):
+        if mode == "norm":
+            frn.fused_reduce_rmsnorm(p, r, g, EPS, residual_out=ro, y=y)
+        else:
+            frn.fused_reduce_rmsnorm_quant_per_group(p, r, g, EPS, 128, mode == "quant_b", residual_out=ro, y=y, q=q,
+                                                     scales=s)
+    torch.cuda.synchronize()
+    print(json.dumps({"case": name, "R": R, "T": T, "H": Hh, "mode": mode, "iters": iters,
+                      "launch": frn.query_launch(T, Hh, R, mode != "norm"),
+                      "bytes_per_call": syn.algorithmic_bytes(R, T, Hh, mode)}))
+
+
 # ------------------------------------------------------------------ main --
 
 def main():
@@ -459,7 +495,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["frn", "reference"], default="frn")
     ap.add_argument("--no-extras", action="store_true", help="skip sweep / large-T / e2e / CPU legs")
+    ap.add_argument("--case", choices=sorted(PROFILE_CASES), help="profiling mode: launch one workload only")
+    ap.add_argument("--iters", type=int, default=3, help="launches in --case mode")
     args = ap.parse_args()
+    if args.case:
+        torch.cuda.set_device(0)
+        run_profile_case(args.case, args.iters)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

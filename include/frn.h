@@ -185,10 +185,15 @@ int frn_version(void);
  * frn_set_ctas_per_row: row kernel only.  0 (default) chooses how many CTAs
  *   of a cluster share a row from T, H and the SM count; 1..8 forces it
  *   (rounded so that no CTA is empty).
+ * frn_set_stream_groups: stream kernel only.  0 (default) chooses how many
+ *   consumer groups (each taking every n-th row of a CTA, so that one group's
+ *   epilogue overlaps the next group's loads) from H; 1..4 forces it, reduced
+ *   where the CTA would exceed 16 warps.
  */
 frn_status frn_set_pdl(int enable);
 frn_status frn_set_kernel(int kernel);
 frn_status frn_set_ctas_per_row(int ctas_per_row);
+frn_status frn_set_stream_groups(int groups);
 
 /*
  * Report the launch a call with these sizes would use on the current device:

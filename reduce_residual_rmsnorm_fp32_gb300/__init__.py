@@ -30,7 +30,7 @@ import torch
 
 __all__ = [
     "FrnError", "fused_reduce_rmsnorm", "fused_reduce_rmsnorm_quant_per_group", "library",
-    "set_pdl", "set_kernel", "set_ctas_per_row", "query_launch", "device_status", "set_test_hooks",
+    "set_pdl", "set_kernel", "set_ctas_per_row", "set_stream_groups", "query_launch", "device_status", "set_test_hooks",
     "status_string", "version", "KERNEL_AUTO", "KERNEL_ROWS", "KERNEL_STREAM",
     "unfused_workspace_bytes", "unfused_reduce_rmsnorm",
     "FRN_OK", "FRN_ERR_INVALID_ARG", "FRN_ERR_UNSUPPORTED", "FRN_ERR_MISALIGNED", "FRN_ERR_CUDA",
@@ -74,6 +74,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_set_ctas_per_row.restype = i32
     lib.frn_set_kernel.argtypes = [i32]
     lib.frn_set_kernel.restype = i32
+    lib.frn_set_stream_groups.argtypes = [i32]
+    lib.frn_set_stream_groups.restype = i32
     lib.frn_query_launch.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                      ctypes.POINTER(i32), ctypes.POINTER(i64)]
     lib.frn_query_launch.restype = i32
@@ -127,6 +129,11 @@ def set_ctas_per_row(n: int) -> None:
 def set_kernel(kind: int) -> None:
     """KERNEL_AUTO (default), KERNEL_ROWS or KERNEL_STREAM."""
     _check(library().frn_set_kernel(int(kind)))
+
+
+def set_stream_groups(groups: int) -> None:
+    """Stream kernel consumer groups: 0 = automatic, 1..4 forced."""
+    _check(library().frn_set_stream_groups(int(groups)))
 
 
 def query_launch(T: int, H: int, R: int, quant: bool = False) -> tuple[int, int, int, int]:
@@ -298,3 +305,4 @@ def unfused_reduce_rmsnorm(partials, residual: torch.Tensor | None, gamma: torch
     if emit_y:
         return (y, q, scales), residual_out
     return (q, scales), residual_out
+

@@ -26,6 +26,7 @@ thread_local char g_detail[256] = "";
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_force_ctas{0};
 std::atomic<int> g_force_kernel{0};
+std::atomic<int> g_force_groups{0};
 std::atomic<int> g_inject_stall{0};
 std::atomic<long long> g_wait_limit_ns{0};
 
@@ -118,20 +119,27 @@ frn::RowPlan choose_rows(long long T, int H, int num_sms) {
     return plan;
 }
 
-// Launch shape of the stream kernel: at most 16 consumer warps with 1, 2 or 4
-// tiles each, as many row-slice slots as fit in 227 KB, one CTA per SM.
+// Launch shape of the stream kernel: 1, 2 or 4 tiles per consumer warp so that
+// a group has at most 8 warps (16 for H > 8192), then as many groups (<= 4) as
+// keep the CTA at 16 warps; as many row-slice slots as fit in 227 KB; one CTA
+// per SM.
 frn::StreamPlan choose_stream(long long T, int H, int num_sms) {
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
-    int tpw = ceil_div(ntiles, frn::kStreamMaxConsumerWarps);
-    tpw = tpw <= 1 ? 1 : (tpw <= 2 ? 2 : 4);
+    const int tpw = ntiles <= 4 ? 1 : (ntiles <= 8 ? 2 : 4);
     frn::StreamPlan plan;
     plan.tiles_per_warp = tpw;
     plan.consumer_warps = ceil_div(ntiles, tpw);
+    int groups = g_force_groups.load(std::memory_order_relaxed);
+    if (groups <= 0) groups = 15 / plan.consumer_warps;
+    if (groups > frn::kStreamMaxGroups) groups = frn::kStreamMaxGroups;
+    if (groups < 1) groups = 1;
+    while (groups > 1 && (groups * plan.consumer_warps + 1) > 16) --groups;
+    plan.groups = groups;
     const int slice = 2 * H;
     int slots = (frn::kStreamSmemLimit - frn::kStreamSmemReserve) / slice;
     if (slots > frn::kStreamMaxSlots) slots = frn::kStreamMaxSlots;
     plan.slots = slots;
-    plan.smem_bytes = frn::stream_smem_bytes(slots, slice);
+    plan.smem_bytes = frn::stream_smem_bytes(slots, slice, groups);
     plan.grid = T < num_sms ? T : num_sms;
     return plan;
 }
@@ -279,6 +287,7 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
     p.eps = c.eps;
     p.nslices = c.R + (c.residual ? 1 : 0);
     p.consumer_warps = splan.consumer_warps;
+    p.groups = splan.groups;
     p.slots = splan.slots;
     p.slice_bytes = 2 * c.H;
     const long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
@@ -447,6 +456,13 @@ FRN_EXPORT frn_status frn_set_kernel(int kernel) {
     return ok();
 }
 
+FRN_EXPORT frn_status frn_set_stream_groups(int groups) {
+    if (groups < 0 || groups > frn::kStreamMaxGroups)
+        return fail(FRN_ERR_INVALID_ARG, "groups=%d must be 0..%d", groups, frn::kStreamMaxGroups);
+    g_force_groups.store(groups, std::memory_order_relaxed);
+    return ok();
+}
+
 FRN_EXPORT frn_status frn_set_test_hooks(int inject_stall, int64_t wait_limit_ns) {
     g_inject_stall.store(inject_stall ? 1 : 0, std::memory_order_relaxed);
     g_wait_limit_ns.store(wait_limit_ns > 0 ? static_cast<long long>(wait_limit_ns) : 0, std::memory_order_relaxed);
@@ -482,7 +498,7 @@ FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* 
     if (kind == kStream) {
         const frn::StreamPlan plan = choose_stream(T, H, sms);
         if (ctas_per_row) *ctas_per_row = 1;
-        if (threads_per_cta) *threads_per_cta = (plan.consumer_warps + 1) * 32;
+        if (threads_per_cta) *threads_per_cta = (plan.groups * plan.consumer_warps + 1) * 32;
         if (grid_ctas) *grid_ctas = plan.grid;
     } else {
         const frn::RowPlan plan = choose_rows(T, H, sms);

@@ -61,7 +61,8 @@ struct Params {
     float eps;
     // stream kernel
     int nslices;             // bulk copies per row: R partials, then the residual if any
-    int consumer_warps;
+    int consumer_warps;      // per consumer group
+    int groups;              // consumer groups, each taking every groups-th row of the CTA
     int slots;               // shared-memory ring slots, one row slice (2*H bytes) each
     int slice_bytes;
     unsigned long long wait_limit_ns;   // bound on every mbarrier wait

@@ -7,12 +7,19 @@
 // ring of shared-memory slots:
 //  * producer warp, one lane: wait until a slot is empty, arm its "full"
 //    mbarrier with the slice's byte count, issue the bulk copy;
-//  * consumer warps (one or more tiles each): wait until the slot is full,
-//    accumulate their vectors from shared memory in slice order (rank order,
-//    residual last), release the slot; after the last slice, run the same
-//    per-vector epilogue as the row kernel (bf16 residual_out, fixed-tree sum
-//    of squares, y, quant), with the tile sums exchanged through shared memory
-//    and one named barrier per row.
+//  * consumer groups of warps (one to four tiles per warp): a group takes every
+//    groups-th row of the CTA's sequence, so while one group runs a row's
+//    epilogue the next group is already accumulating the following row.  A
+//    group waits until a slot is full, accumulates its vectors from shared
+//    memory in slice order (rank order, residual last), releases the slot, and
+//    after the last slice runs the same per-vector epilogue as the row kernel
+//    (bf16 residual_out, fixed-tree sum of squares, y, quant), with the tile
+//    sums exchanged through shared memory and one named barrier (its own) per
+//    row.  Each group owns its own sub-ring of slots (the producer writes row i
+//    into group i % groups' sub-ring), so every slot's barriers have exactly one
+//    consumer, which takes the slot's fills in order -- the property the parity
+//    waits rely on (a group that could wait on a slot one fill ahead of another
+//    group would see the earlier phase's parity and pass too early).
 // The ring holds ~220 KB, so up to that many bytes per SM stay in flight while
 // the consumers reduce, normalise and store -- independent of registers.
 //
@@ -28,15 +35,15 @@
 
 namespace frn {
 
-constexpr int kStreamMaxConsumerWarps = 16;
-constexpr int kStreamThreads = (kStreamMaxConsumerWarps + 1) * 32;
+constexpr int kStreamMaxConsumerWarps = 16;   // one group (H > 8192)
+constexpr int kStreamMaxGroups = 4;
 constexpr int kStreamMaxSlots = 32;
 constexpr int kStreamSmemLimit = 232448;     // 227 KB opt-in per CTA on sm_100-class parts
-constexpr int kStreamSmemReserve = 2048;     // barriers, tile sums, flags (<= 16*32 + 512 + 16)
+constexpr int kStreamSmemReserve = 3072;     // barriers, tile sums, flags (<= 16*32 + 4*512 + 16)
 
-__host__ __device__ constexpr int stream_smem_bytes(int slots, int slice_bytes) {
-    // data ring | full[slots], empty[slots] | tile sums [2][kMaxTiles] | abort flag
-    return slots * slice_bytes + 16 * slots + 2 * kMaxTiles * 4 + 16;
+__host__ __device__ constexpr int stream_smem_bytes(int slots, int slice_bytes, int groups) {
+    // data ring | full[slots], empty[slots] | tile sums [groups][2][kMaxTiles] | abort flag
+    return slots * slice_bytes + 16 * slots + groups * 2 * kMaxTiles * 4 + 16;
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting or
@@ -56,27 +63,31 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
-// Named barrier 1 over the consumer warps, OR-reducing a predicate.
-__device__ __forceinline__ bool consumers_sync_or(bool pred, int nthreads) {
+// Named barrier `id` over `nthreads` consumer threads, OR-reducing a predicate.
+__device__ __forceinline__ bool consumers_sync_or(int id, bool pred, int nthreads) {
     uint32_t out;
     asm volatile(
         "{\n\t.reg .pred pin, pout;\n\t"
         "setp.ne.u32 pin, %1, 0;\n\t"
-        "bar.red.or.pred pout, 1, %2, pin;\n\t"
+        "bar.red.or.pred pout, %2, %3, pin;\n\t"
         "selp.u32 %0, 1, 0, pout;\n\t}"
-        : "=r"(out) : "r"((uint32_t)pred), "r"(nthreads) : "memory");
+        : "=r"(out) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
     return out != 0;
 }
 
-template <int TPW, int MODE>
-__global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __grid_constant__ Params p) {
+// MAXTHREADS is the launch bound: 512 (16 warps, 128 registers a thread) for
+// every shape but one group of 16 consumer warps (H > 8192), which needs 544.
+template <int TPW, int MODE, int MAXTHREADS>
+__global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int NC = p.consumer_warps;
+    const int G = p.groups;
     const int S = p.slots;
+    const int SG = S / G;              // slots of each group's sub-ring
     const uint32_t slice = static_cast<uint32_t>(p.slice_bytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slice);
     float* tsum = reinterpret_cast<float*>(bars + 2 * S);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tsum + 2 * kMaxTiles);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tsum + G * 2 * kMaxTiles);
     const uint32_t data0 = smem_addr(smem);
     const uint32_t full0 = smem_addr(bars);
     const uint32_t empty0 = full0 + 8u * S;
@@ -96,14 +107,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __g
     // before it has completed.
     grid_dependency_wait();
 
-    if (warp == NC) {
+    if (warp == G * NC) {
         // ------------------------------------------------------- producer --
         if (lane == 0) {
-            int slot = 0;
-            uint32_t ph = 0, issued = 0, issued_par = 0;
+            uint32_t issued = 0, issued_par = 0;
+            int used[kStreamMaxGroups] = {0, 0, 0, 0};   // slices issued into each group's sub-ring
             bool ok = true;
-            for (long long row = blockIdx.x; ok && row < p.T; row += gridDim.x) {
+            int i = 0;
+            for (long long row = blockIdx.x; ok && row < p.T; row += gridDim.x, ++i) {
+                const int grp = i % G;
                 for (int k = 0; k < p.nslices; ++k) {
+                    const int n = used[grp]++;
+                    const int slot = grp * SG + n % SG;
+                    const uint32_t ph = static_cast<uint32_t>(n / SG) & 1u;
                     if (!wait_bounded(empty0 + 8u * slot, ph ^ 1u, abort_flag, p.wait_limit_ns, p.error_word)) {
                         ok = false;
                         break;
@@ -115,10 +131,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __g
                         bulk_g2s(data0 + static_cast<uint32_t>(slot) * slice, src, slice, full0 + 8u * slot);
                         issued |= 1u << slot;
                         issued_par = (issued_par & ~(1u << slot)) | (ph << slot);
-                    }
-                    if (++slot == S) {
-                        slot = 0;
-                        ph ^= 1u;
                     }
                 }
             }
@@ -141,27 +153,33 @@ __global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __g
     }
 
     // ----------------------------------------------------------- consumers --
-    // gamma stays in registers, except with 4 tiles per warp (H > 8192), where
-    // 17 warps leave 96 registers a thread and gamma is re-read (L2) per row.
+    const int grp = warp / NC;
+    const int lw = warp - grp * NC;            // warp index within the group
+    // gamma stays in registers for 1-2 tiles a warp; with 4 it is re-read from
+    // cache per row to keep the consumer inside its register budget.
     constexpr bool kGammaInRegs = TPW < 4;
     int jt[TPW];
     bool vt[TPW];
     uint4 g[kGammaInRegs ? TPW : 1];
 #pragma unroll
     for (int t = 0; t < TPW; ++t) {
-        const int tile = warp + t * NC;
+        const int tile = lw + t * NC;
         jt[t] = tile * kTileVecs + lane;
         vt[t] = jt[t] < p.nvec;
         if constexpr (kGammaInRegs) g[t] = ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
     }
+    float* gsum = tsum + grp * 2 * kMaxTiles;
     const int ng = p.H / kGroup;
-    int slot = 0;
+    int lslot = 0;                     // position in this group's sub-ring
     uint32_t ph = 0;
     int prow = 0;
     bool ok = true;
-    for (long long row = blockIdx.x; row < p.T; row += gridDim.x) {
+    // this group's rows: the (grp + groups*m)-th rows of the CTA's sequence
+    for (long long row = blockIdx.x + static_cast<long long>(grp) * gridDim.x; row < p.T;
+         row += static_cast<long long>(G) * gridDim.x) {
         float acc[TPW][8];
         for (int k = 0; k < p.nslices; ++k) {
+            const int slot = grp * SG + lslot;
             const bool got = ok && wait_bounded(full0 + 8u * slot, ph, abort_flag, p.wait_limit_ns, p.error_word);
             ok = got;
             const uint4* src = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(slot) * slice);
@@ -176,8 +194,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __g
             }
             __syncwarp();
             if (lane == 0 && got) mbar_arrive(empty0 + 8u * slot);
-            if (++slot == S) {
-                slot = 0;
+            if (++lslot == SG) {
+                lslot = 0;
                 ph ^= 1u;
             }
         }
@@ -193,11 +211,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __g
             if (ok && vt[t]) p.residual_out[rbase + jt[t]] = rov[t];
             float xs[8];
             const float s = tile_sumsq(rov[t], xs);
-            if (lane == 0 && warp + t * NC < p.ntiles) tsum[prow * kMaxTiles + warp + t * NC] = s;
+            if (lane == 0 && lw + t * NC < p.ntiles) gsum[prow * kMaxTiles + lw + t * NC] = s;
         }
-        if (consumers_sync_or(!ok || *abort_flag != 0, NC * 32)) break;
-        const float lo = lane < p.ntiles ? tsum[prow * kMaxTiles + lane] : 0.0f;
-        const float hi = lane + 32 < p.ntiles ? tsum[prow * kMaxTiles + lane + 32] : 0.0f;
+        if (consumers_sync_or(1 + grp, !ok || *abort_flag != 0, NC * 32)) break;
+        const float lo = lane < p.ntiles ? gsum[prow * kMaxTiles + lane] : 0.0f;
+        const float hi = lane + 32 < p.ntiles ? gsum[prow * kMaxTiles + lane + 32] : 0.0f;
         const float rstd = row_rstd(lo, hi, p.H, p.eps);
 #pragma unroll
         for (int t = 0; t < TPW; ++t) {
@@ -224,27 +242,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1) frn_stream_kernel(const __g
 
 struct StreamPlan {
     int tiles_per_warp;
-    int consumer_warps;
+    int consumer_warps;   // per group
+    int groups;
     int slots;
     int smem_bytes;
     long long grid;
 };
 
-template <int TPW, int MODE>
+template <int TPW, int MODE, int MAXTHREADS>
 cudaError_t launch_stream_one(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl) {
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(frn_stream_kernel<TPW, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kStreamSmemLimit);
+        e = cudaFuncSetAttribute(frn_stream_kernel<TPW, MODE, MAXTHREADS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmemLimit);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>((plan.consumer_warps + 1) * 32), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>((plan.groups * plan.consumer_warps + 1) * 32), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -252,15 +271,17 @@ cudaError_t launch_stream_one(const Params& p, const StreamPlan& plan, cudaStrea
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, frn_stream_kernel<TPW, MODE>, p);
+    return cudaLaunchKernelEx(&cfg, frn_stream_kernel<TPW, MODE, MAXTHREADS>, p);
 }
 
 template <int MODE>
 cudaError_t launch_stream(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl) {
+    if ((plan.groups * plan.consumer_warps + 1) * 32 > 512)
+        return launch_stream_one<4, MODE, (kStreamMaxConsumerWarps + 1) * 32>(p, plan, stream, pdl);
     switch (plan.tiles_per_warp) {
-        case 1: return launch_stream_one<1, MODE>(p, plan, stream, pdl);
-        case 2: return launch_stream_one<2, MODE>(p, plan, stream, pdl);
-        default: return launch_stream_one<4, MODE>(p, plan, stream, pdl);
+        case 1: return launch_stream_one<1, MODE, 512>(p, plan, stream, pdl);
+        case 2: return launch_stream_one<2, MODE, 512>(p, plan, stream, pdl);
+        default: return launch_stream_one<4, MODE, 512>(p, plan, stream, pdl);
     }
 }
 

@@ -18,11 +18,13 @@ from frn_testlib import assert_residual_exact, assert_y_close, dev_bf16, host_bi
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_copy_times_out_and_context_survives():
+@pytest.mark.parametrize("groups", [0, 1])
+def test_stalled_copy_times_out_and_context_survives(groups):
     inp = syn.make_inputs(2, 400, 4096, seed=80)
     p, r, g = dev_bf16(inp.partials), dev_bf16(inp.residual), dev_bf16(inp.gamma)
     assert frn.device_status(clear=True) in (frn.FRN_OK, frn.FRN_ERR_TIMEOUT)
     frn.set_kernel(frn.KERNEL_STREAM)
+    frn.set_stream_groups(groups)
     try:
         frn.set_test_hooks(inject_stall=True, wait_limit_ns=50_000_000)
         frn.fused_reduce_rmsnorm(p, r, g, inp.eps)
@@ -36,6 +38,7 @@ def test_stalled_copy_times_out_and_context_survives():
         torch.cuda.synchronize()
     finally:
         frn.set_kernel(frn.KERNEL_AUTO)
+        frn.set_stream_groups(0)
     assert frn.device_status() == frn.FRN_OK
     rro, ry = oracle.Oracle().reduce_rmsnorm(inp.partials, inp.residual, inp.gamma, inp.eps)
     assert_residual_exact(host_bits(ro), rro)

@@ -251,3 +251,18 @@ def test_eps_matters():
     inp = syn.make_inputs(2, 8, 2048, seed=9, partial_std=1e-3, residual_std=1e-3)
     check_norm(syn.Inputs(inp.partials, inp.residual, inp.gamma, 1e-6), "eps ~ mean square")
     check_norm(syn.Inputs(inp.partials, inp.residual, inp.gamma, 0.5), "eps dominant")
+
+
+@pytest.mark.parametrize("groups", [1, 2, 3, 4])
+@pytest.mark.parametrize("R,T,H", [(4, 301, 4096), (8, 157, 7168), (2, 400, 1024), (3, 97, 256)])
+def test_stream_consumer_groups(groups, R, T, H):
+    """Every consumer-group count gives the same bits, and they match the oracle."""
+    inp = syn.make_inputs(R, T, H, seed=11 + groups, partial_std=0.5)
+    frn.set_kernel(frn.KERNEL_STREAM)
+    frn.set_stream_groups(groups)
+    try:
+        check_quant(inp, f"stream groups={groups} R={R} T={T} H={H}") if H % 128 == 0 else \
+            check_norm(inp, f"stream groups={groups} R={R} T={T} H={H}")
+    finally:
+        frn.set_stream_groups(0)
+        frn.set_kernel(frn.KERNEL_AUTO)
