@@ -159,6 +159,39 @@ frn_status frn_unfused_reduce_rmsnorm(const void* const* partials, int R,
                                       int stages, void* workspace, int64_t workspace_bytes,
                                       frn_stream_t stream);
 
+/*
+ * No-allocation variant of frn_unfused_reduce_rmsnorm.  (The pages have no
+ * counterpart: it exists for callers of this library that cannot allocate
+ * device memory on the call path -- code running during CUDA-graph capture in
+ * the default capture mode, where cudaMalloc is not allowed; serving engines
+ * that hand nearly all device memory to their own pool at start-up; plugins
+ * given raw pointers and no allocator.)
+ *
+ * Same arguments and results as frn_unfused_reduce_rmsnorm, without the
+ * workspace: the scratch is a fixed array of FRN_STATIC_WORKSPACE_BYTES (16 MiB)
+ * inside the library's device image, which every GPU that loads the library
+ * holds until the process exits.  Nothing is allocated or freed by any call.
+ *  - Sizes whose scratch (frn_unfused_workspace_bytes) exceeds the array are
+ *    rejected with FRN_ERR_UNSUPPORTED, e.g. 3 stages with quant and no y at
+ *    H = 7168 fit up to T = 390.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array and leaves its last contents
+ *    there (nothing needs to start at zero: each call overwrites what it reads).
+ *    Calls that can overlap on the GPU -- on different streams without ordering
+ *    between them, or from several host threads -- race on it; order them, or
+ *    use frn_unfused_reduce_rmsnorm with separate workspaces.
+ */
+#define FRN_STATIC_WORKSPACE_BYTES (16LL << 20)
+
+frn_status frn_unfused_reduce_rmsnorm_noalloc(const void* const* partials, int R,
+                                              const void* residual, const void* gamma,
+                                              void* residual_out, void* y,
+                                              void* q_e4m3, float* scales,
+                                              int64_t T, int H, float eps, int group_size,
+                                              int stages, frn_stream_t stream);
+
 /* Static text for a status code. */
 const char* frn_status_string(frn_status s);
 

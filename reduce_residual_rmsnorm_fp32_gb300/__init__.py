@@ -32,7 +32,8 @@ __all__ = [
     "FrnError", "fused_reduce_rmsnorm", "fused_reduce_rmsnorm_quant_per_group", "library",
     "set_pdl", "set_kernel", "set_ctas_per_row", "set_stream_groups", "query_launch", "device_status", "set_test_hooks",
     "status_string", "version", "KERNEL_AUTO", "KERNEL_ROWS", "KERNEL_STREAM",
-    "unfused_workspace_bytes", "unfused_reduce_rmsnorm",
+    "unfused_workspace_bytes", "unfused_reduce_rmsnorm", "unfused_reduce_rmsnorm_noalloc",
+    "STATIC_WORKSPACE_BYTES",
     "FRN_OK", "FRN_ERR_INVALID_ARG", "FRN_ERR_UNSUPPORTED", "FRN_ERR_MISALIGNED", "FRN_ERR_CUDA",
     "FRN_ERR_TIMEOUT", "MAX_PARTIALS", "MAX_HIDDEN", "QUANT_GROUP",
 ]
@@ -42,6 +43,7 @@ KERNEL_AUTO, KERNEL_ROWS, KERNEL_STREAM = 0, 1, 2
 MAX_PARTIALS = 16
 MAX_HIDDEN = 16384
 QUANT_GROUP = 128
+STATIC_WORKSPACE_BYTES = 16 << 20
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfrn.so")
 _lib = None
@@ -88,6 +90,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_unfused_reduce_rmsnorm.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, vp, vp, i64, i32, f32, i32,
                                                i32, vp, i64, vp]
     lib.frn_unfused_reduce_rmsnorm.restype = i32
+    lib.frn_unfused_reduce_rmsnorm_noalloc.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, vp, vp, i64, i32,
+                                                       f32, i32, i32, vp]
+    lib.frn_unfused_reduce_rmsnorm_noalloc.restype = i32
     return lib
 
 
@@ -306,3 +311,21 @@ def unfused_reduce_rmsnorm(partials, residual: torch.Tensor | None, gamma: torch
         return (y, q, scales), residual_out
     return (q, scales), residual_out
 
+
+def unfused_reduce_rmsnorm_noalloc(partials, residual: torch.Tensor | None, gamma: torch.Tensor,
+                                   eps: float = 1e-6, *, stages: int = 2, residual_out: torch.Tensor,
+                                   y: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                                   scales: torch.Tensor | None = None, group_size: int = QUANT_GROUP, stream=None):
+    """The unfused paths with the library's fixed static scratch instead of a
+    workspace, for callers that cannot allocate device memory.  The caller passes
+    every output (nothing is allocated here either); results as
+    ``unfused_reduce_rmsnorm``.  The first call on a device should come before
+    any stream capture, and calls that can overlap on the GPU race on the shared
+    scratch."""
+    ptrs, R, T, H, dev = _partials(partials)
+    arr = (ctypes.c_void_p * R)(*ptrs)
+    with torch.cuda.device(dev):
+        st = library().frn_unfused_reduce_rmsnorm_noalloc(
+            arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales), T, H,
+            float(eps), int(group_size), int(stages), _stream(stream, dev))
+    _check(st)

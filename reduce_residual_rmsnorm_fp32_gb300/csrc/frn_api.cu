@@ -422,6 +422,68 @@ FRN_EXPORT frn_status frn_unfused_reduce_rmsnorm(const void* const* partials, in
     return run_unfused(c, stages, stream);
 }
 
+// ------------------------------------------------ no-allocation variant --
+//
+// The unfused paths need scratch: the fp32 sum of the partials and, without a
+// y output, the bf16 y.  Some callers cannot allocate it: code running while a
+// CUDA graph is being captured in the default (global) capture mode, where
+// cudaMalloc is not allowed; serving engines that give nearly all device memory
+// to their own pool at start-up and forbid allocation on the hot path; plugins
+// handed raw pointers and no allocator.  For them this variant keeps its
+// scratch in the array below, a fixed part of the library's device image: every
+// GPU that loads the library holds FRN_STATIC_WORKSPACE_BYTES of it until the
+// process exits, and no call allocates or frees anything.
+static __device__ __align__(256) unsigned char g_frn_static_workspace[FRN_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+std::atomic<void*> g_static_ws_addr[kMaxDevices];
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+frn_status static_workspace(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(FRN_ERR_UNSUPPORTED, "device %d out of range", dev);
+    void* a = g_static_ws_addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        e = cudaGetSymbolAddress(&a, g_frn_static_workspace);
+        if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_static_ws_addr[dev].store(a, std::memory_order_release);
+    }
+    *out = a;
+    return FRN_OK;
+}
+
+}  // namespace
+
+FRN_EXPORT frn_status frn_unfused_reduce_rmsnorm_noalloc(const void* const* partials, int R, const void* residual,
+                                                         const void* gamma, void* residual_out, void* y,
+                                                         void* q_e4m3, float* scales, int64_t T, int H, float eps,
+                                                         int group_size, int stages, frn_stream_t stream) {
+    const int quant = q_e4m3 || scales ? (y ? 2 : 1) : 0;
+    if (!(stages == 2 || (stages == 3 && quant)))
+        return fail(FRN_ERR_INVALID_ARG, "stages=%d: 2, or 3 with quant", stages);
+    const long long need = unfused_workspace(T, H, stages, quant != 0, y != nullptr);
+    if (need > FRN_STATIC_WORKSPACE_BYTES)
+        return fail(FRN_ERR_UNSUPPORTED,
+                    "needs %lld bytes of scratch; the static workspace holds %lld (pass your own to "
+                    "frn_unfused_reduce_rmsnorm instead)",
+                    need, static_cast<long long>(FRN_STATIC_WORKSPACE_BYTES));
+    void* ws = nullptr;
+    if (T > 0) {
+        frn_status st = static_workspace(&ws);
+        if (st != FRN_OK) return st;
+    }
+    // The array is fully overwritten before it is read (the fp32 sum, then y),
+    // so nothing in it has to start at zero.
+    const Call c{partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps,
+                 quant ? group_size : FRN_QUANT_GROUP, quant, ws, FRN_STATIC_WORKSPACE_BYTES, 0};
+    return run_unfused(c, stages, stream);
+}
+
 FRN_EXPORT const char* frn_status_string(frn_status s) {
     switch (s) {
         case FRN_OK: return "FRN_OK";
