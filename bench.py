@@ -332,32 +332,41 @@ def measure_fusion(frn, R, T, Hh, seed, hbm, outlier=False, partial_std=0.5):
 
 
 def measure_e2e(frn, steps: int):
-    """The decode step through the public API from pinned host buffers."""
-    host = {}
-    for i, T in enumerate(DECODE_T):
-        inp = syn.config_decode(T, seed=500 + i)
-        host[T] = (torch.from_numpy(inp.partials.view(np.int16)).view(torch.bfloat16).pin_memory(),
-                   torch.from_numpy(inp.residual.view(np.int16)).view(torch.bfloat16).pin_memory(),
-                   torch.empty((T, H), dtype=torch.bfloat16).pin_memory(),
-                   torch.empty((T, H), dtype=torch.bfloat16).pin_memory())
-    gamma_h = torch.from_numpy(syn.config_decode(8).gamma.view(np.int16)).view(torch.bfloat16).pin_memory()
-    dev = {T: (torch.empty_like(h[0], device="cuda"), torch.empty_like(h[1], device="cuda"),
-               torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
-               torch.empty((T, H), dtype=torch.bfloat16, device="cuda")) for T, h in host.items()}
-    gamma_d = torch.empty_like(gamma_h, device="cuda")
-    h2d = gamma_h.numel() * 2 + sum(h[0].numel() * 2 + h[1].numel() * 2 for h in host.values())
-    d2h = sum(2 * T * H * 2 for T in DECODE_T)
+    """The decode step through the public API from pinned host memory.  Every
+    step copies all of its inputs (the four T values' partials and residuals,
+    and gamma) host->device in one copy from one pinned buffer, makes the four
+    fused calls, and reads all outputs (residual_out and y) back in one copy."""
+    inps = [syn.config_decode(T, seed=500 + i) for i, T in enumerate(DECODE_T)]
+    in_parts = []
+    for inp in inps:
+        in_parts += [inp.partials.reshape(-1), inp.residual.reshape(-1)]
+    in_parts.append(inps[0].gamma)
+    flat_in = np.concatenate(in_parts).view(np.int16)
+    host_in = torch.from_numpy(flat_in).pin_memory()
+    n_out = sum(2 * T * H for T in DECODE_T)
+    host_out = torch.empty((n_out,), dtype=torch.int16).pin_memory()
+    dev_in = torch.empty_like(host_in, device="cuda")
+    dev_out = torch.empty((n_out,), dtype=torch.int16, device="cuda")
+    # device views, in the order of the packed buffers
+    views, off, ooff = [], 0, 0
+    for T in DECODE_T:
+        npart, nres = R_DEC * T * H, T * H
+        p = dev_in[off:off + npart].view(torch.bfloat16).view(R_DEC, T, H)
+        r = dev_in[off + npart:off + npart + nres].view(torch.bfloat16).view(T, H)
+        off += npart + nres
+        ro = dev_out[ooff:ooff + T * H].view(torch.bfloat16).view(T, H)
+        y = dev_out[ooff + T * H:ooff + 2 * T * H].view(torch.bfloat16).view(T, H)
+        ooff += 2 * T * H
+        views.append((p, r, ro, y))
+    gamma_d = dev_in[off:off + H].view(torch.bfloat16)
+    h2d = host_in.numel() * 2
+    d2h = host_out.numel() * 2
 
     def one_step():
-        gamma_d.copy_(gamma_h, non_blocking=True)
-        for T in DECODE_T:
-            hp, hr, hro, hy = host[T]
-            dp, dr, dro, dy = dev[T]
-            dp.copy_(hp, non_blocking=True)
-            dr.copy_(hr, non_blocking=True)
-            frn.fused_reduce_rmsnorm(dp, dr, gamma_d, EPS, residual_out=dro, y=dy)
-            hro.copy_(dro, non_blocking=True)
-            hy.copy_(dy, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
+        for p, r, ro, y in views:
+            frn.fused_reduce_rmsnorm(p, r, gamma_d, EPS, residual_out=ro, y=y)
+        host_out.copy_(dev_out, non_blocking=True)
 
     for _ in range(3):
         one_step()

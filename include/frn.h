@@ -131,6 +131,26 @@ frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* partials, int
                                                 frn_stream_t stream);
 
 /*
+ * The adjacent steps of the same layer, on the same kernels ("ROCm AITER fused
+ * all-reduce + RMSNorm", vLLM PR 37646 summary, implementation breakdown item
+ * 2: the rms_norm and fused_add_rms_norm patterns).
+ *
+ * frn_fused_add_rmsnorm: one activation x plus the residual, i.e.
+ *   fused_reduce_rmsnorm with R = 1: residual_out = bf16(f32(x) + f32(residual)),
+ *   y = RMSNorm(residual_out).  residual may be NULL (zeros) and residual_out
+ *   may equal residual.
+ * frn_rmsnorm: y = bf16((f32(x) * rstd) * f32(gamma)), rstd over f32(x) + 0.0
+ *   (so a -0.0 input element gives +0.0); nothing else is written.
+ * Arguments, layouts, limits and errors as for fused_reduce_rmsnorm.
+ */
+frn_status frn_fused_add_rmsnorm(const void* x, const void* residual, const void* gamma,
+                                 void* residual_out, void* y, int64_t T, int H, float eps,
+                                 frn_stream_t stream);
+
+frn_status frn_rmsnorm(const void* x, const void* gamma, void* y, int64_t T, int H, float eps,
+                       frn_stream_t stream);
+
+/*
  * Unfused comparison paths: the same outputs, bit for bit, computed the way an
  * unfused layer would, to measure what fusion saves ("AMD fused
  * AllReduce-RMSNorm quant kernel", SGLang PR 24651 summary, implementation
@@ -211,7 +231,7 @@ int frn_version(void);
  *   the kernel's prologue may overlap the tail of the previous kernel on the
  *   stream; the kernel still waits for that kernel's completion before its
  *   first global-memory access.  0 launches plainly.
- * frn_set_kernel: 0 (default) picks the kernel from T and the SM count;
+ * frn_set_kernel: 0 (default) picks the kernel from T, H and the SM count;
  *   1 forces the row kernel (one row per thread-block cluster, for few rows),
  *   2 forces the stream kernel (persistent, one CTA per SM, rows streamed
  *   through shared memory with TMA bulk copies, for many rows).

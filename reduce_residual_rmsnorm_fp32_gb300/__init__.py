@@ -32,7 +32,7 @@ __all__ = [
     "FrnError", "fused_reduce_rmsnorm", "fused_reduce_rmsnorm_quant_per_group", "library",
     "set_pdl", "set_kernel", "set_ctas_per_row", "set_stream_groups", "query_launch", "device_status", "set_test_hooks",
     "status_string", "version", "KERNEL_AUTO", "KERNEL_ROWS", "KERNEL_STREAM",
-    "unfused_workspace_bytes", "unfused_reduce_rmsnorm", "unfused_reduce_rmsnorm_noalloc",
+    "fused_add_rmsnorm", "rmsnorm", "unfused_workspace_bytes", "unfused_reduce_rmsnorm", "unfused_reduce_rmsnorm_noalloc",
     "STATIC_WORKSPACE_BYTES",
     "FRN_OK", "FRN_ERR_INVALID_ARG", "FRN_ERR_UNSUPPORTED", "FRN_ERR_MISALIGNED", "FRN_ERR_CUDA",
     "FRN_ERR_TIMEOUT", "MAX_PARTIALS", "MAX_HIDDEN", "QUANT_GROUP",
@@ -85,6 +85,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_device_status.restype = i32
     lib.frn_set_test_hooks.argtypes = [i32, i64]
     lib.frn_set_test_hooks.restype = i32
+    lib.frn_fused_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i32, f32, vp]
+    lib.frn_fused_add_rmsnorm.restype = i32
+    lib.frn_rmsnorm.argtypes = [vp, vp, vp, i64, i32, f32, vp]
+    lib.frn_rmsnorm.restype = i32
     lib.frn_unfused_workspace_bytes.argtypes = [i64, i32, i32, i32, i32]
     lib.frn_unfused_workspace_bytes.restype = i64
     lib.frn_unfused_reduce_rmsnorm.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, vp, vp, i64, i32, f32, i32,
@@ -329,3 +333,38 @@ def unfused_reduce_rmsnorm_noalloc(partials, residual: torch.Tensor | None, gamm
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales), T, H,
             float(eps), int(group_size), int(stages), _stream(stream, dev))
     _check(st)
+
+
+def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None, gamma: torch.Tensor, eps: float = 1e-6, *,
+                      residual_out: torch.Tensor | None = None, y: torch.Tensor | None = None, stream=None):
+    """residual_out = x + residual (fp32, one rounding), y = RMSNorm(residual_out); returns (y, residual_out)."""
+    T, H = x.shape
+    dev = x.device
+    _check_tensor(x, "x", torch.bfloat16, (T, H), dev)
+    if residual is not None:
+        _check_tensor(residual, "residual", torch.bfloat16, (T, H), dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
+    residual_out = torch.empty_like(x) if residual_out is None else residual_out
+    y = torch.empty_like(x) if y is None else y
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
+    _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
+    with torch.cuda.device(dev):
+        st = library().frn_fused_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), T,
+                                             H, float(eps), _stream(stream, dev))
+    _check(st)
+    return y, residual_out
+
+
+def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, *, y: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """y = RMSNorm(x) with weight gamma (bf16 in and out, fp32 arithmetic)."""
+    T, H = x.shape
+    dev = x.device
+    _check_tensor(x, "x", torch.bfloat16, (T, H), dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
+    y = torch.empty_like(x) if y is None else y
+    _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
+    with torch.cuda.device(dev):
+        st = library().frn_rmsnorm(_ptr(x), _ptr(gamma), _ptr(y), T, H, float(eps), _stream(stream, dev))
+    _check(st)
+    return y

@@ -103,11 +103,15 @@ frn::RowPlan choose_rows(long long T, int H, int num_sms) {
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
     if (forced > 0) {
         C = forced < cmin ? cmin : (forced > cmax ? cmax : forced);
+    } else if (cmin == 1) {
+        // The row fits one CTA: no cluster (a cluster launch and its barriers
+        // cost more than spreading a small row gains).
+        C = 1;
     } else {
-        // Few rows: spread each row over more SMs (down to 4 warps per CTA)
-        // until the rows alone give about two CTAs per SM.
+        // The row needs a cluster anyway: spread it over more SMs (down to 4
+        // warps per CTA) while the rows still leave SMs idle.
         C = cmin;
-        while (C < cmax && T * C < 2LL * num_sms && ceil_div(ntiles, C + 1) >= 4) ++C;
+        while (C < cmax && T * (C + 1) <= num_sms && ceil_div(ntiles, C + 1) >= 4) ++C;
     }
     const int tpc = ceil_div(ntiles, C);
     C = ceil_div(ntiles, tpc);   // no empty CTA
@@ -144,12 +148,15 @@ frn::StreamPlan choose_stream(long long T, int H, int num_sms) {
     return plan;
 }
 
-// Which kernel: the row kernel while the rows alone cannot keep every SM
-// streaming, the stream kernel beyond.
-int choose_kind(long long T, int num_sms) {
+// Which kernel: a row that fits one CTA (H <= 4096) streams best through the
+// row kernel at any T (several CTAs, i.e. rows, in flight per SM); a wider row
+// goes to the stream kernel once there is a row per SM.
+int choose_kind(long long T, int H, int num_sms) {
     const int forced = g_force_kernel.load(std::memory_order_relaxed);
     if (forced == kRows || forced == kStream) return forced;
-    return T >= 2LL * num_sms ? kStream : kRows;
+    const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
+    if (ntiles <= frn::kMaxTilesPerCta) return kRows;
+    return T >= num_sms ? kStream : kRows;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -185,6 +192,7 @@ struct Call {
     void* workspace;
     long long workspace_bytes;
     long long workspace_needed;
+    bool no_residual_out;   // plain RMSNorm: residual_out is not written
 };
 
 // Everything that can be checked on the host: scalars, pointers, alignment,
@@ -217,12 +225,13 @@ frn_status validate(const Call& c, bool* empty) {
         if (!aligned(c.partials[r], 16)) return fail(FRN_ERR_MISALIGNED, "partials[%d] not 16-byte aligned", r);
     }
     if (!c.gamma) return fail(FRN_ERR_INVALID_ARG, "gamma is NULL");
-    if (!c.residual_out) return fail(FRN_ERR_INVALID_ARG, "residual_out is NULL");
+    if (!c.residual_out && !c.no_residual_out) return fail(FRN_ERR_INVALID_ARG, "residual_out is NULL");
     if (c.quant != 1 && !c.y) return fail(FRN_ERR_INVALID_ARG, "y is NULL");
     if (c.quant && (!c.q || !c.scales)) return fail(FRN_ERR_INVALID_ARG, "q / scales is NULL");
     if (!aligned(c.gamma, 16)) return fail(FRN_ERR_MISALIGNED, "gamma not 16-byte aligned");
     if (c.residual && !aligned(c.residual, 16)) return fail(FRN_ERR_MISALIGNED, "residual not 16-byte aligned");
-    if (!aligned(c.residual_out, 16)) return fail(FRN_ERR_MISALIGNED, "residual_out not 16-byte aligned");
+    if (c.residual_out && !aligned(c.residual_out, 16))
+        return fail(FRN_ERR_MISALIGNED, "residual_out not 16-byte aligned");
     if (c.y && !aligned(c.y, 16)) return fail(FRN_ERR_MISALIGNED, "y not 16-byte aligned");
     if (c.quant && !aligned(c.q, 16)) return fail(FRN_ERR_MISALIGNED, "q not 16-byte aligned");
     if (c.quant && !aligned(c.scales, 4)) return fail(FRN_ERR_MISALIGNED, "scales not 4-byte aligned");
@@ -240,7 +249,7 @@ frn_status validate(const Call& c, bool* empty) {
     const long long act = 2LL * T * H;
     Range outs[5];
     int nout = 0;
-    outs[nout++] = range_of(c.residual_out, act, "residual_out");
+    if (c.residual_out) outs[nout++] = range_of(c.residual_out, act, "residual_out");
     if (c.y) outs[nout++] = range_of(c.y, act, "y");
     if (c.quant) {
         outs[nout++] = range_of(c.q, T * static_cast<long long>(H), "q");
@@ -258,7 +267,7 @@ frn_status validate(const Call& c, bool* empty) {
         if (overlap(outs[a], range_of(c.gamma, 2LL * H, "gamma")))
             return fail(FRN_ERR_INVALID_ARG, "%s overlaps gamma", outs[a].name);
         if (c.residual && overlap(outs[a], range_of(c.residual, act, "residual"))) {
-            const bool in_place = (a == 0) && c.residual_out == c.residual;
+            const bool in_place = c.residual_out != nullptr && (a == 0) && c.residual_out == c.residual;
             if (!in_place) return fail(FRN_ERR_INVALID_ARG, "%s overlaps residual", outs[a].name);
         }
     }
@@ -300,7 +309,7 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // The fused epilogue (one kernel).  quant as in Call; the kernel writes c.y
 // when it is not NULL.
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
-    const int kind = choose_kind(c.T, sms);
+    const int kind = choose_kind(c.T, c.H, sms);
     const frn::RowPlan rplan = choose_rows(c.T, c.H, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
@@ -392,7 +401,7 @@ FRN_EXPORT frn_status fused_reduce_rmsnorm(const void* const* partials, int R, c
                                            const void* gamma, void* residual_out, void* y, int64_t T,
                                            int H, float eps, frn_stream_t stream) {
     const Call c{partials, R, residual, gamma, residual_out, y, nullptr, nullptr, T, H, eps, FRN_QUANT_GROUP,
-                 0, nullptr, 0, 0};
+                 0, nullptr, 0, 0, false};
     return run(c, stream);
 }
 
@@ -402,7 +411,24 @@ FRN_EXPORT frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* pa
                                                            float* scales, int64_t T, int H, float eps,
                                                            int group_size, frn_stream_t stream) {
     const Call c{partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps, group_size,
-                 y ? 2 : 1, nullptr, 0, 0};
+                 y ? 2 : 1, nullptr, 0, 0, false};
+    return run(c, stream);
+}
+
+FRN_EXPORT frn_status frn_fused_add_rmsnorm(const void* x, const void* residual, const void* gamma,
+                                            void* residual_out, void* y, int64_t T, int H, float eps,
+                                            frn_stream_t stream) {
+    const void* parts[1] = {x};
+    const Call c{x ? parts : nullptr, 1, residual, gamma, residual_out, y, nullptr, nullptr, T, H, eps,
+                 FRN_QUANT_GROUP, 0, nullptr, 0, 0, false};
+    return run(c, stream);
+}
+
+FRN_EXPORT frn_status frn_rmsnorm(const void* x, const void* gamma, void* y, int64_t T, int H, float eps,
+                                  frn_stream_t stream) {
+    const void* parts[1] = {x};
+    const Call c{x ? parts : nullptr, 1, nullptr, gamma, nullptr, y, nullptr, nullptr, T, H, eps,
+                 FRN_QUANT_GROUP, 0, nullptr, 0, 0, true};
     return run(c, stream);
 }
 
@@ -418,7 +444,7 @@ FRN_EXPORT frn_status frn_unfused_reduce_rmsnorm(const void* const* partials, in
                                                  frn_stream_t stream) {
     const int quant = q_e4m3 || scales ? (y ? 2 : 1) : 0;
     const Call c{partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps,
-                 quant ? group_size : FRN_QUANT_GROUP, quant, workspace, workspace_bytes, 0};
+                 quant ? group_size : FRN_QUANT_GROUP, quant, workspace, workspace_bytes, 0, false};
     return run_unfused(c, stages, stream);
 }
 
@@ -480,7 +506,7 @@ FRN_EXPORT frn_status frn_unfused_reduce_rmsnorm_noalloc(const void* const* part
     // The array is fully overwritten before it is read (the fp32 sum, then y),
     // so nothing in it has to start at zero.
     const Call c{partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps,
-                 quant ? group_size : FRN_QUANT_GROUP, quant, ws, FRN_STATIC_WORKSPACE_BYTES, 0};
+                 quant ? group_size : FRN_QUANT_GROUP, quant, ws, FRN_STATIC_WORKSPACE_BYTES, 0, false};
     return run_unfused(c, stages, stream);
 }
 
@@ -555,7 +581,7 @@ FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* 
     int sms = 0;
     frn_status st = sm_count(&sms);
     if (st != FRN_OK) return st;
-    const int kind = choose_kind(T, sms);
+    const int kind = choose_kind(T, H, sms);
     if (kernel) *kernel = kind;
     if (kind == kStream) {
         const frn::StreamPlan plan = choose_stream(T, H, sms);

@@ -47,7 +47,7 @@ struct Params {
     const uint4* partials[kMaxPartials];
     const uint4* residual;   // nullptr: zeros
     const uint4* gamma;
-    uint4* residual_out;
+    uint4* residual_out;     // nullptr: not stored (plain RMSNorm)
     uint4* y;                // bf16 output (kNorm, kQuantB)
     uint2* q;                // e4m3 codes, 8 per vector (kQuantA, kQuantB)
     float* scales;           // [T, H/128]
@@ -228,13 +228,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  ::"r"(bar), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// One bounded try: the thread may sleep in the instruction until the phase
+// completes or about `hint_ns` pass, so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = 20000) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
     return ok != 0;
 }
 

@@ -55,13 +55,15 @@ __global__ void __launch_bounds__(kMaxThreads) frn_row_kernel(const __grid_const
         if (r < p.R) add8(acc, raw[r]);
     add8(acc, res);
     const uint4 ro = pack8(acc);
-    if (valid) p.residual_out[off] = ro;
 
     float x[8];
     const float s = tile_sumsq(ro, x);
     if (lane == 0) tile_sum[warp] = s;
     __syncwarp();
 
+    // Every global store of this thread comes after the cluster arrivals below:
+    // a release arrival waits for all of the thread's earlier memory operations,
+    // and it only has to cover the tile sums and the DSMEM reads.
     float lo, hi;   // tile slots `lane` and `lane + 32` of the row
     if constexpr (CLUSTER) {
         cluster_arrive_release();
@@ -78,6 +80,7 @@ __global__ void __launch_bounds__(kMaxThreads) frn_row_kernel(const __grid_const
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
         hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     }
+    if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
     const float rstd = row_rstd(lo, hi, p.H, p.eps);
     const uint4 yb = rms_y(x, rstd, g);
     if constexpr (MODE != kQuantA) {

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
 #pragma unroll
         for (int t = 0; t < TPW; ++t) {
             rov[t] = pack8(acc[t]);
-            if (ok && vt[t]) p.residual_out[rbase + jt[t]] = rov[t];
+            if (ok && vt[t] && p.residual_out != nullptr) p.residual_out[rbase + jt[t]] = rov[t];
             float xs[8];
             const float s = tile_sumsq(rov[t], xs);
             if (lane == 0 && lw + t * NC < p.ntiles) gsum[prow * kMaxTiles + lw + t * NC] = s;
