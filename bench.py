@@ -66,6 +66,34 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def kernel_source_hash() -> str:
+    """sha256 of the CUDA sources, to tell whether a recorded ncu capture still
+    describes the kernels being timed."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_fp32_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(case: str):
+    """DRAM bytes per launch (read + write) of `case` from the committed ncu
+    summary, or None when the summary is missing or was taken on other kernel
+    sources."""
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == case and parts[2] == kernel_source_hash():
+            return int(parts[1])
+    return None
+
+
 def step_bytes():
     return sum(syn.algorithmic_bytes(R_DEC, T, H, "norm") for T in DECODE_T)
 
@@ -567,7 +595,8 @@ def main():
         b64 = dec["64"]["bytes"]
         ach = b64 / t64 / 1e9
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(ach / hbm, 4), "traffic": None,
+                    "frac": round(ach / hbm, 4), "traffic": recorded_traffic("decode64"),
+                    "algorithmic_bytes": b64, "kernel_sources": kernel_source_hash(),
                     "kernel": "frn_row_kernel<8, norm, cluster> at T=64 (the step's largest call)",
                     "peak_kind": peak_kind}
         large = [measure_rows(frn, 8, syn.sweep_tokens(m), "norm", 20000 + i, hbm)
