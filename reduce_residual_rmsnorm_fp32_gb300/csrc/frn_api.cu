@@ -94,13 +94,22 @@ frn_status status_word(unsigned int** out) {
 // Launch shape of the row kernel.  A row's ntiles warp tiles go to C CTAs of
 // a cluster.  The results do not depend on this choice (the reduction tree is
 // fixed by H).
-frn::RowPlan choose_rows(long long T, int H, int num_sms) {
+frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     const int nvec = H / frn::kVecElems;
     const int ntiles = ceil_div(nvec, frn::kTileVecs);
     const int cmin = ceil_div(ntiles, frn::kMaxTilesPerCta);
     const int cmax = ntiles < 8 ? ntiles : 8;
     int C;
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
+    if (forced == 1 && ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8) {
+        // one wide CTA (up to 1024 threads) per row, no cluster
+        frn::RowPlan plan;
+        plan.ctas_per_row = 1;
+        plan.tiles_per_cta = ntiles;
+        plan.threads = ntiles * 32;
+        plan.grid = T;
+        return plan;
+    }
     if (forced > 0) {
         C = forced < cmin ? cmin : (forced > cmax ? cmax : forced);
     } else if (cmin == 1) {
@@ -125,19 +134,23 @@ frn::RowPlan choose_rows(long long T, int H, int num_sms) {
 
 // Launch shape of the stream kernel: 1, 2 or 4 tiles per consumer warp so that
 // a group has at most 8 warps (16 for H > 8192), then as many groups (<= 4) as
-// keep the CTA at 16 warps; as many row-slice slots as fit in 227 KB; one CTA
-// per SM.
-frn::StreamPlan choose_stream(long long T, int H, int num_sms) {
+// keep the CTA within its warp budget; as many row-slice slots as fit in
+// 227 KB; one CTA per SM.  The budget is 22 warps (the 704-thread variant, 80
+// registers) when rows have few slices (R + 1 <= 4): there the consumers'
+// per-row epilogue, not HBM, sets the pace and more groups overlap more of it.
+// With more slices a deeper sub-ring per group pays more: 16 warps.
+frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
     const int tpw = ntiles <= 4 ? 1 : (ntiles <= 8 ? 2 : 4);
     frn::StreamPlan plan;
     plan.tiles_per_warp = tpw;
     plan.consumer_warps = ceil_div(ntiles, tpw);
+    const int max_warps = (tpw == 4 && nslices <= 4) ? frn::kStreamMaxThreads / 32 : 16;
     int groups = g_force_groups.load(std::memory_order_relaxed);
-    if (groups <= 0) groups = 15 / plan.consumer_warps;
+    if (groups <= 0) groups = (max_warps - 1) / plan.consumer_warps;
     if (groups > frn::kStreamMaxGroups) groups = frn::kStreamMaxGroups;
     if (groups < 1) groups = 1;
-    while (groups > 1 && (groups * plan.consumer_warps + 1) > 16) --groups;
+    while (groups > 1 && (groups * plan.consumer_warps + 1) > max_warps) --groups;
     plan.groups = groups;
     const int slice = 2 * H;
     int slots = (frn::kStreamSmemLimit - frn::kStreamSmemReserve) / slice;
@@ -310,8 +323,8 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // when it is not NULL.
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, sms);
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, sms);
-    const frn::StreamPlan splan = choose_stream(c.T, c.H, sms);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
+    const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
     unsigned int* status = nullptr;
@@ -379,8 +392,8 @@ frn_status run_unfused(Call c, int stages, frn_stream_t stream) {
                          : reinterpret_cast<uint4*>(ws + (need_x ? 4LL * c.T * c.H : 0));
     Call norm = c;
     norm.y = ytarget;
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, sms);
-    const frn::StreamPlan splan = choose_stream(c.T, c.H, sms);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
+    const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     frn::Params p = make_params(norm, rplan, splan, nullptr);
     cudaError_t e = cudaSuccess;
     if (need_x) {
@@ -584,12 +597,12 @@ FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* 
     const int kind = choose_kind(T, H, sms);
     if (kernel) *kernel = kind;
     if (kind == kStream) {
-        const frn::StreamPlan plan = choose_stream(T, H, sms);
+        const frn::StreamPlan plan = choose_stream(T, H, R + 1, sms);
         if (ctas_per_row) *ctas_per_row = 1;
         if (threads_per_cta) *threads_per_cta = (plan.groups * plan.consumer_warps + 1) * 32;
         if (grid_ctas) *grid_ctas = plan.grid;
     } else {
-        const frn::RowPlan plan = choose_rows(T, H, sms);
+        const frn::RowPlan plan = choose_rows(T, H, R, sms);
         if (ctas_per_row) *ctas_per_row = plan.ctas_per_row;
         if (threads_per_cta) *threads_per_cta = plan.threads;
         if (grid_ctas) *grid_ctas = plan.grid;

@@ -135,6 +135,13 @@ __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Relaxed arrival that must follow the computation of `after`: the dummy input
+// makes the compiler keep that computation (and the loads it consumed) ahead
+// of the arrival, and in-order issue keeps the hardware from reordering them.
+__device__ __forceinline__ void cluster_arrive_relaxed_after(float after) {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned; // %0" ::"f"(after) : "memory");
+}
+
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -186,11 +193,43 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// acc[2i] += f32(lo half of w), acc[2i+1] += f32(hi half): the mixed-precision
+// add takes the bf16 straight from the register half.  Widening bf16 is exact,
+// so this is the same single-rounded fp32 add as unpacking first.
+__device__ __forceinline__ void add2_bf16(float& a0, float& a1, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(w));
+}
+
 __device__ __forceinline__ void add8(float (&acc)[8], const uint4 v) {
-    float f[8];
-    unpack8(v, f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+    add2_bf16(acc[0], acc[1], v.x);
+    add2_bf16(acc[2], acc[3], v.y);
+    add2_bf16(acc[4], acc[5], v.z);
+    add2_bf16(acc[6], acc[7], v.w);
+}
+
+// s = fma(x_lo, x_lo, s); s = fma(x_hi, x_hi, s) with bf16 x: the product of two
+// bf16 values is exact in fp32, so this is the fp32 FMA of the widened values.
+__device__ __forceinline__ float sumsq2_bf16(float s, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, lo, lo, %0;\n\t"
+        "fma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+        : "+f"(s) : "r"(w));
+    return s;
+}
+
+// max |element| of a packed bf16 pair set, as a bf16 pair (exact).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m, uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b32 a;\n\t"
+        "abs.bf16x2 a, %2;\n\t"
+        "max.bf16x2 %0, %1, a;\n\t}"
+        : "=r"(r) : "r"(m), "r"(w));
+    return r;
 }
 
 __device__ __forceinline__ float butterfly_sum(float v) {
@@ -250,13 +289,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 // ------------------------------------------------- per-vector arithmetic ----
 
-// Sum of squares of one tile: x <- f32(ro); FMA chain over the 8 elements of
-// this lane's vector; xor butterfly over the 32 lanes.
-__device__ __forceinline__ float tile_sumsq(const uint4 ro, float (&x)[8]) {
-    unpack8(ro, x);
+// Sum of squares of one tile: an fp32 FMA chain over the 8 elements of this
+// lane's bf16 vector, in element order; xor butterfly over the 32 lanes.
+__device__ __forceinline__ float tile_sumsq(const uint4 ro) {
     float s = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s = __fmaf_rn(x[i], x[i], s);
+    s = sumsq2_bf16(s, ro.x);
+    s = sumsq2_bf16(s, ro.y);
+    s = sumsq2_bf16(s, ro.z);
+    s = sumsq2_bf16(s, ro.w);
     return butterfly_sum(s);
 }
 
@@ -266,9 +306,10 @@ __device__ __forceinline__ float row_rstd(float lo, float hi, int H, float eps) 
     return __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(H)), eps));
 }
 
-// y = bf16((x * rstd) * gamma) for one vector.
-__device__ __forceinline__ uint4 rms_y(const float (&x)[8], float rstd, const uint4 g) {
-    float gf[8], yv[8];
+// y = bf16((x * rstd) * gamma) for one vector of bf16 x.
+__device__ __forceinline__ uint4 rms_y(const uint4 xb, float rstd, const uint4 g) {
+    float x[8], gf[8], yv[8];
+    unpack8(xb, x);
     unpack8(g, gf);
 #pragma unroll
     for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(__fmul_rn(x[i], rstd), gf[i]);
@@ -281,12 +322,24 @@ __device__ __forceinline__ uint4 rms_y(const float (&x)[8], float rstd, const ui
 __device__ __forceinline__ void quant8(const uint4 yb, uint2& qq, float& sc) {
     float yq[8];
     unpack8(yb, yq);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(yq[i]));
+    uint32_t mp = absmax_bf16x2(0u, yb.x);
+    mp = absmax_bf16x2(mp, yb.y);
+    mp = absmax_bf16x2(mp, yb.z);
+    mp = absmax_bf16x2(mp, yb.w);
+    float amax = fmaxf(__uint_as_float(mp << 16), __uint_as_float(mp & 0xFFFF0000u));
 #pragma unroll
     for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
-    sc = __fdiv_rn(amax, 448.0f);
+    if (amax >= 0x1p-60f) {
+        // absmax / 448, correctly rounded, without a divide: RN(absmax * RN(1/448))
+        // and one FMA correction (Markstein's theorem); checked exhaustively for
+        // every bf16 significand of absmax.
+        constexpr float kInv448 = 1.0f / 448.0f;
+        const float q0 = __fmul_rn(amax, kInv448);
+        const float rem = __fmaf_rn(-448.0f, q0, amax);
+        sc = __fmaf_rn(rem, kInv448, q0);
+    } else {
+        sc = __fdiv_rn(amax, 448.0f);
+    }
     qq = make_uint2(0u, 0u);
     if (sc != 0.0f) {
         float qv[8];

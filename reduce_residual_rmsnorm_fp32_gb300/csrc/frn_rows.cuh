@@ -16,10 +16,12 @@
 namespace frn {
 
 // RMAX is the unrolled partial count (R <= RMAX; loads beyond R are predicated
-// off).  CLUSTER == false is the single-CTA row (no cluster barriers).
-template <int RMAX, int MODE, bool CLUSTER>
-__global__ void __launch_bounds__(kMaxThreads) frn_row_kernel(const __grid_constant__ Params p) {
-    __shared__ float tile_sum[kMaxTilesPerCta];
+// off).  CLUSTER == false is the single-CTA row (no cluster barriers).  MAXT is
+// the launch bound: 512 threads (16 tiles), or 1024 for a single-CTA row of up
+// to 32 tiles (H <= 8192, R <= 8: 64 registers a thread).
+template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
+__global__ void __launch_bounds__(MAXT) frn_row_kernel(const __grid_constant__ Params p) {
+    __shared__ float tile_sum[MAXT / 32];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -56,8 +58,7 @@ __global__ void __launch_bounds__(kMaxThreads) frn_row_kernel(const __grid_const
     add8(acc, res);
     const uint4 ro = pack8(acc);
 
-    float x[8];
-    const float s = tile_sumsq(ro, x);
+    const float s = tile_sumsq(ro);
     if (lane == 0) tile_sum[warp] = s;
     __syncwarp();
 
@@ -71,18 +72,21 @@ __global__ void __launch_bounds__(kMaxThreads) frn_row_kernel(const __grid_const
         const int tpc = p.tiles_per_cta;
         lo = lane < p.ntiles ? ld_dsmem(&tile_sum[lane % tpc], lane / tpc) : 0.0f;
         hi = lane + 32 < p.ntiles ? ld_dsmem(&tile_sum[(lane + 32) % tpc], (lane + 32) / tpc) : 0.0f;
-        __syncwarp();
-        // Done reading the other CTAs' shared memory; they may exit once all
-        // CTAs have arrived here (matching wait at the end).
-        cluster_arrive_release();
     } else {
         __syncthreads();
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
         hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     }
-    if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
+    // rstd consumes lo and hi, so the DSMEM reads have completed before the
+    // relaxed arrival below tells the other CTAs they may exit (matching wait
+    // at the end); no release, hence no wait on anything else.
     const float rstd = row_rstd(lo, hi, p.H, p.eps);
-    const uint4 yb = rms_y(x, rstd, g);
+    if constexpr (CLUSTER) {
+        __syncwarp();
+        cluster_arrive_relaxed_after(rstd);
+    }
+    if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
+    const uint4 yb = rms_y(ro, rstd, g);
     if constexpr (MODE != kQuantA) {
         if (valid) p.y[off] = yb;
     }
@@ -109,7 +113,7 @@ struct RowPlan {
     long long grid;
 };
 
-template <int RMAX, int MODE, bool CLUSTER>
+template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
 cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
@@ -132,12 +136,19 @@ cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t st
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, frn_row_kernel<RMAX, MODE, CLUSTER>, p);
+    return cudaLaunchKernelEx(&cfg, frn_row_kernel<RMAX, MODE, CLUSTER, MAXT>, p);
 }
 
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
+    if (plan.threads > kMaxThreads) {
+        // one wide CTA per row (the host only plans this for R <= 8)
+        if (p.R <= 1) return launch_row_one<1, MODE, false, 1024>(p, plan, stream, pdl);
+        if (p.R <= 2) return launch_row_one<2, MODE, false, 1024>(p, plan, stream, pdl);
+        if (p.R <= 4) return launch_row_one<4, MODE, false, 1024>(p, plan, stream, pdl);
+        return launch_row_one<8, MODE, false, 1024>(p, plan, stream, pdl);
+    }
     const bool cl = plan.ctas_per_row > 1;
 #define FRN_DISPATCH_R(RM)                                                        \
     return cl ? launch_row_one<RM, MODE, true>(p, plan, stream, pdl)             \

@@ -36,6 +36,7 @@
 namespace frn {
 
 constexpr int kStreamMaxConsumerWarps = 16;   // one group (H > 8192)
+constexpr int kStreamMaxThreads = 704;        // 22 warps
 constexpr int kStreamMaxGroups = 4;
 constexpr int kStreamMaxSlots = 32;
 constexpr int kStreamSmemLimit = 232448;     // 227 KB opt-in per CTA on sm_100-class parts
@@ -75,8 +76,9 @@ __device__ __forceinline__ bool consumers_sync_or(int id, bool pred, int nthread
     return out != 0;
 }
 
-// MAXTHREADS is the launch bound: 512 (16 warps, 128 registers a thread) for
-// every shape but one group of 16 consumer warps (H > 8192), which needs 544.
+// MAXTHREADS is the launch bound: 512 (16 warps, up to 128 registers a
+// thread), 544 (17 warps: one group of 16 consumer warps for H > 8192, or two
+// of 8) or 704 (22 warps: three groups of 7 for H = 7168, 80 registers).
 template <int TPW, int MODE, int MAXTHREADS>
 __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -209,8 +211,7 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
         for (int t = 0; t < TPW; ++t) {
             rov[t] = pack8(acc[t]);
             if (ok && vt[t] && p.residual_out != nullptr) p.residual_out[rbase + jt[t]] = rov[t];
-            float xs[8];
-            const float s = tile_sumsq(rov[t], xs);
+            const float s = tile_sumsq(rov[t]);
             if (lane == 0 && lw + t * NC < p.ntiles) gsum[prow * kMaxTiles + lw + t * NC] = s;
         }
         if (consumers_sync_or(1 + grp, !ok || *abort_flag != 0, NC * 32)) break;
@@ -219,10 +220,8 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
         const float rstd = row_rstd(lo, hi, p.H, p.eps);
 #pragma unroll
         for (int t = 0; t < TPW; ++t) {
-            float x[8];
-            unpack8(rov[t], x);
             const uint4 gt = kGammaInRegs ? g[kGammaInRegs ? t : 0] : ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
-            const uint4 yb = rms_y(x, rstd, gt);
+            const uint4 yb = rms_y(rov[t], rstd, gt);
             if constexpr (MODE != kQuantA) {
                 if (vt[t]) p.y[rbase + jt[t]] = yb;
             }
@@ -276,8 +275,9 @@ cudaError_t launch_stream_one(const Params& p, const StreamPlan& plan, cudaStrea
 
 template <int MODE>
 cudaError_t launch_stream(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl) {
-    if ((plan.groups * plan.consumer_warps + 1) * 32 > 512)
-        return launch_stream_one<4, MODE, (kStreamMaxConsumerWarps + 1) * 32>(p, plan, stream, pdl);
+    const int threads = (plan.groups * plan.consumer_warps + 1) * 32;
+    if (threads > 544) return launch_stream_one<4, MODE, kStreamMaxThreads>(p, plan, stream, pdl);
+    if (threads > 512) return launch_stream_one<4, MODE, 544>(p, plan, stream, pdl);
     switch (plan.tiles_per_warp) {
         case 1: return launch_stream_one<1, MODE, 512>(p, plan, stream, pdl);
         case 2: return launch_stream_one<2, MODE, 512>(p, plan, stream, pdl);

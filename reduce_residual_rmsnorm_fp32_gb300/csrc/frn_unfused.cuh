@@ -65,8 +65,7 @@ __global__ void __launch_bounds__(512) frn_addnorm_kernel(const __grid_constant_
         add8(acc, ld_coherent(p.residual + off, valid && p.residual != nullptr));
         rov[t] = pack8(acc);
         if (valid) p.residual_out[off] = rov[t];
-        float xs[8];
-        const float s = tile_sumsq(rov[t], xs);
+        const float s = tile_sumsq(rov[t]);
         if (lane == 0 && tile < p.ntiles) tile_sum[tile] = s;
     }
     __syncthreads();
@@ -77,9 +76,7 @@ __global__ void __launch_bounds__(512) frn_addnorm_kernel(const __grid_constant_
     for (int t = 0; t < TPW; ++t) {
         const int j = (warp + t * nw) * kTileVecs + lane;
         const bool valid = j < p.nvec;
-        float x[8];
-        unpack8(rov[t], x);
-        const uint4 yb = rms_y(x, rstd, ld_keep(p.gamma + (valid ? j : 0), valid));
+        const uint4 yb = rms_y(rov[t], rstd, ld_keep(p.gamma + (valid ? j : 0), valid));
         if (valid) y[row * p.nvec + j] = yb;
     }
     launch_dependents();

@@ -1,4 +1,5 @@
-"""The quant epilogue divides y by the group scale with one correctly rounded
+"""The quant epilogue computes the group scale absmax / 448 as RN(absmax *
+RN(1/448)) plus one FMA correction, and divides y by the group scale with one correctly rounded
 reciprocal per group and one FMA correction step (Markstein's theorem) instead
 of an IEEE divide per element.  This CPU test replays that sequence in exact
 rational arithmetic for every bf16 significand of y against every significand
@@ -48,3 +49,16 @@ def test_fma_corrected_quotient_is_correctly_rounded():
             rem = rn32(y - s * q0)                         # __fmaf_rn(-s, q0, y)
             q1 = rn32(q0 + rem * rs)                       # __fmaf_rn(rem, rs, q0)
             assert q1 == rn32(y / s), (y, s)
+
+
+def test_fma_corrected_scale_is_correctly_rounded():
+    """absmax / 448 for every bf16 significand of absmax (the binade of absmax
+    relative to 448 only shifts the exponent)."""
+    c = rn32(F(1, 448))                                     # the constant 1.0f / 448.0f
+    for m in range(128):
+        a = F(128 + m, 128)
+        for shift in range(0, 10):
+            aa = a * 2 ** shift
+            q0 = rn32(aa * c)
+            rem = rn32(aa - 448 * q0)
+            assert rn32(q0 + rem * c) == rn32(aa / 448), (m, shift)
