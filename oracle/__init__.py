@@ -59,6 +59,14 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_e4m3_to_double.restype = ctypes.c_double
     lib.oracle_e4m3_from_double.argtypes = [ctypes.c_double]
     lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+    lib.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1_to_double.restype = ctypes.c_double
+    lib.oracle_e2m1_from_double.argtypes = [ctypes.c_double]
+    lib.oracle_e2m1_from_double.restype = ctypes.c_uint8
+    lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e8m0_to_double.restype = ctypes.c_double
+    lib.oracle_mxfp4.argtypes = [u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_mxfp4.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -125,6 +133,32 @@ class Oracle:
         ro, y = self.reduce_rmsnorm(partials, residual, gamma, eps, True, threads)
         q, s = self.quant_per_group(y, group_size, threads)
         return ro, y, q, s
+
+    def mxfp4(self, y: np.ndarray, threads: int = 1):
+        """y uint16 [T,H] bf16 bits -> (q uint8 [T,H/2] packed E2M1, scales uint8 [T,H/32] E8M0)."""
+        y = np.ascontiguousarray(y, dtype=np.uint16)
+        T, H = y.shape
+        q = np.empty((T, H // 2), dtype=np.uint8)
+        scales = np.empty((T, H // 32), dtype=np.uint8)
+        rc = self.lib.oracle_mxfp4(self._ptr(y), T, H, self._ptr(q), self._ptr(scales), int(threads))
+        if rc != 0:
+            raise ValueError("oracle_mxfp4 rejected its arguments")
+        return q, scales
+
+    def reduce_rmsnorm_mxfp4(self, partials, residual, gamma, eps, threads=1):
+        """MXFP4 epilogue: returns (residual_out, y, q, scales)."""
+        ro, y = self.reduce_rmsnorm(partials, residual, gamma, eps, True, threads)
+        q, s = self.mxfp4(y, threads)
+        return ro, y, q, s
+
+    def e2m1_to_double(self, c: int) -> float:
+        return self.lib.oracle_e2m1_to_double(int(c) & 0xF)
+
+    def e2m1_from_double(self, v: float) -> int:
+        return int(self.lib.oracle_e2m1_from_double(float(v)))
+
+    def e8m0_to_double(self, c: int) -> float:
+        return self.lib.oracle_e8m0_to_double(int(c) & 0xFF)
 
     # scalar format helpers (used by the pins)
     def bf16_to_double(self, b: int) -> float:

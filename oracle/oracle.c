@@ -40,7 +40,11 @@
  *    q = e4m3fn_rn_satfinite(fp32(y / s)), both divisions IEEE fp32 (the
  *    precision the kernel decides the code in); s == 0 gives q = 0;
  *  - scales are [T, H/group] row-major fp32; e4m3 is the OCP "fn" format
- *    (bias 7, max 448, no infinities, NaN = S.1111.111).
+ *    (bias 7, max 448, no infinities, NaN = S.1111.111);
+ *  - the MXFP4 output (a third fused variant the AITER fix names without a
+ *    format) follows the OCP Microscaling Formats v1.0 conversion: blocks of
+ *    32, shared E8M0 exponent floor(log2(absmax)) - 2, E2M1 elements rounded
+ *    to nearest even and saturated; element 2i in the low nibble of a byte.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -fopenmp -shared -fPIC.
  * ffp-contract=off keeps every fp32 add a separately rounded IEEE add.
@@ -140,6 +144,40 @@ uint8_t oracle_e4m3_from_double(double v)
     int e = ex - 1;                                    /* -6 .. 8 */
     int m = (int)ldexp(r, 3 - e) - 8;                  /* r = (8 + m) * 2^(e-3) */
     return sign | (uint8_t)((e + 7) << 3) | (uint8_t)m;
+}
+
+/* OCP Microscaling (MX) v1.0 FP4 element type E2M1: 1 sign bit, 2 exponent
+ * bits (bias 1), 1 mantissa bit; exponent field 0 holds zero and the subnormal
+ * 0.5; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; no infinities, no NaN. */
+double oracle_e2m1_to_double(uint8_t c)
+{
+    int s = (c >> 3) & 1;
+    int e = (c >> 1) & 0x3;
+    int m = c & 0x1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* Round to nearest even on the E2M1 grid, saturating to +-6. */
+uint8_t oracle_e2m1_from_double(double v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0;
+    double a = fabs(v);
+    double r = (isnan(v) || isinf(a)) ? 6.0 : round_to_grid(a, 2, 0);
+    if (r > 6.0) r = 6.0;
+    if (r == 0.0) return sign;
+    if (r < 1.0) return sign | 0x1;                    /* 0.5: subnormal */
+    int ex;
+    (void)frexp(r, &ex);
+    int e = ex - 1;                                    /* 0 .. 2 */
+    int m = (int)ldexp(r, 1 - e) - 2;                  /* r = (2 + m) * 2^(e-1) */
+    return sign | (uint8_t)((e + 1) << 1) | (uint8_t)m;
+}
+
+/* MX scale type E8M0: 2^(code - 127); code 0xFF is NaN. */
+double oracle_e8m0_to_double(uint8_t c)
+{
+    return c == 0xFF ? NAN : ldexp(1.0, (int)c - 127);
 }
 
 static inline float bf16_to_f32(uint16_t b) { return (float)oracle_bf16_to_double(b); }
@@ -247,6 +285,61 @@ int oracle_quant_per_group(const uint16_t* y, int64_t T, int H, int group,
     (void)threads;
 #endif
     for (int64_t t = 0; t < T; ++t) quant_row(y, H, group, t, q, scales);
+    return 0;
+}
+
+/* MXFP4 (OCP MX v1.0: block size 32, E8M0 scale, E2M1 elements) of a bf16
+ * [T][H] activation, blocks of 32 consecutive elements along H:
+ *   shared_exp = floor(log2(max |y| over the block)) - 2   (2 = emax of E2M1),
+ *                clamped to the E8M0 range [-127, 127];
+ *   X = 2^shared_exp;  P_i = e2m1_rn_satfinite(y_i / X).
+ * An all-zero block gets scale code 0 (2^-127) and zero elements.
+ * q: [T][H/2] bytes, element 2i in the low nibble; scales: [T][H/32] E8M0. */
+static void mxfp4_row(const uint16_t* y, int H, int64_t t, uint8_t* q, uint8_t* scales)
+{
+    int nb = H / 32;
+    for (int b = 0; b < nb; ++b) {
+        const uint16_t* yb = y + t * (int64_t)H + (int64_t)b * 32;
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i) {
+            double v = fabs(oracle_bf16_to_double(yb[i]));
+            if (v > amax) amax = v;
+        }
+        int shared_exp = -127;
+        if (amax > 0.0) {
+            int ex;
+            (void)frexp(amax, &ex);                    /* amax = f * 2^ex, f in [0.5, 1) */
+            shared_exp = (ex - 1) - 2;
+            if (shared_exp < -127) shared_exp = -127;
+            if (shared_exp > 127) shared_exp = 127;
+        }
+        scales[t * (int64_t)nb + b] = (uint8_t)(shared_exp + 127);
+        uint8_t* qb = q + t * (int64_t)(H / 2) + (int64_t)b * 16;
+        for (int i = 0; i < 16; ++i) {
+            uint8_t lo = 0, hi = 0;
+            if (amax > 0.0) {
+                lo = oracle_e2m1_from_double(ldexp(oracle_bf16_to_double(yb[2 * i]), -shared_exp));
+                hi = oracle_e2m1_from_double(ldexp(oracle_bf16_to_double(yb[2 * i + 1]), -shared_exp));
+            }
+            qb[i] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+int oracle_mxfp4(const uint16_t* y, int64_t T, int H, uint8_t* q, uint8_t* scales, int threads)
+{
+    if (!y || !q || !scales || T < 0 || H < 32 || H % 32) return -1;
+    if (fegetround() != FE_TONEAREST) return -1;
+#ifdef _OPENMP
+    if (threads > 1) {
+        #pragma omp parallel for num_threads(threads) schedule(static)
+        for (int64_t t = 0; t < T; ++t) mxfp4_row(y, H, t, q, scales);
+        return 0;
+    }
+#else
+    (void)threads;
+#endif
+    for (int64_t t = 0; t < T; ++t) mxfp4_row(y, H, t, q, scales);
     return 0;
 }
 

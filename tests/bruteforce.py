@@ -35,11 +35,30 @@ def _e4m3_fraction(code: int):
     return -v if s else v
 
 
+def _e2m1_fraction(code: int) -> Fraction:
+    s, e, m = (code >> 3) & 1, (code >> 1) & 0x3, code & 0x1
+    v = Fraction(m, 2) if e == 0 else (1 + Fraction(m, 2)) * Fraction(2) ** (e - 1)
+    return -v if s else v
+
+
 # Non-negative finite codes in increasing value order.
 _BF16_POS = [(_bf16_fraction(c), c) for c in range(0x0000, 0x7F80)]
 _BF16_VALS = [v for v, _ in _BF16_POS]
 _E4M3_POS = [(_e4m3_fraction(c), c) for c in range(0x00, 0x7F)]
 _E4M3_VALS = [v for v, _ in _E4M3_POS]
+_E2M1_POS = [(_e2m1_fraction(c), c) for c in range(0x0, 0x8)]
+_E2M1_VALS = [v for v, _ in _E2M1_POS]
+
+
+def e2m1_value(code: int) -> Fraction:
+    return _e2m1_fraction(int(code))
+
+
+def nearest_e2m1_satfinite(x) -> int:
+    """Exact RNE of a real to E2M1 with saturation to +-6, by exhaustive search."""
+    x = Fraction(x)
+    sign = 0x8 if x < 0 else 0
+    return sign | _nearest(_E2M1_VALS, _E2M1_POS, abs(x), allow_overflow_code=None)
 
 
 def bf16_value(code: int) -> Fraction:
@@ -141,3 +160,31 @@ def quant_per_group(y: np.ndarray, group: int = 128):
                 else:
                     q[t, g * group + i] = nearest_e4m3_satfinite(Fraction(float(np.float32(v / s))))
     return q, s_out
+
+
+def mxfp4(y: np.ndarray):
+    """Brute-force MXFP4 of bf16 bits [T, H]: the shared exponent from the exact
+    binary logarithm of the block's absmax (no library log), codes by exhaustive
+    search; element 2i in the low nibble."""
+    T, H = y.shape
+    q = np.zeros((T, H // 2), dtype=np.uint8)
+    sc = np.zeros((T, H // 32), dtype=np.uint8)
+    for t in range(T):
+        for b in range(H // 32):
+            vals = [bf16_value(y[t, b * 32 + i]) for i in range(32)]
+            amax = max(abs(v) for v in vals)
+            if amax == 0:
+                e = -127
+            else:
+                e = 0
+                while Fraction(2) ** (e + 1) <= amax:
+                    e += 1
+                while Fraction(2) ** e > amax:
+                    e -= 1
+                e = max(-127, min(127, e - 2))
+            sc[t, b] = e + 127
+            for i in range(16):
+                lo = nearest_e2m1_satfinite(vals[2 * i] / Fraction(2) ** e) if amax else 0
+                hi = nearest_e2m1_satfinite(vals[2 * i + 1] / Fraction(2) ** e) if amax else 0
+                q[t, b * 16 + i] = lo | (hi << 4)
+    return q, sc

@@ -354,4 +354,82 @@ def pin_omp_matches_serial(o):
         assert np.array_equal(u, v)
 
 
+# ------------------------------------------------------------------ MXFP4 --
+
+def pin_golden_e2m1_e8m0(o):
+    g = _read_golden("e2m1_e8m0_ocp_mx_points.txt")
+    for code, expr in g["e2m1"]:
+        v = _eval(expr)
+        got = o.e2m1_to_double(int(code, 16))
+        assert got == v and math.copysign(1, got) == math.copysign(1, v), (code, expr, got)
+        assert o.e2m1_from_double(v) == int(code, 16), (code, expr)
+    for expr, code in g["round"]:
+        assert o.e2m1_from_double(_eval(expr)) == int(code, 16), (expr, code)
+    for code, expr in g["e8m0"]:
+        assert o.e8m0_to_double(int(code, 16)) == _eval(expr), (code, expr)
+
+
+def pin_e2m1_rounding_bruteforce(o):
+    """Random values and every midpoint of adjacent E2M1 codes vs exhaustive search."""
+    rng = np.random.default_rng(51)
+    xs = list(rng.uniform(-9, 9, 2000)) + list(np.exp2(rng.uniform(-6, 3.5, 1000)))
+    pos = [bf.e2m1_value(c) for c in range(8)]
+    for a, b in zip(pos[:-1], pos[1:]):
+        m = (a + b) / 2
+        xs += [float(m), float(-m), float(m) + 2 ** -30, float(m) - 2 ** -30]
+    for x in xs:
+        assert o.e2m1_from_double(float(x)) == bf.nearest_e2m1_satfinite(Fraction(float(x))), x
+
+
+def _mx_block_y(amax_sig: float, e: int, n: int, seed: int):
+    rng = np.random.default_rng(seed)
+    y = (rng.uniform(-1, 1, (1, n)) * amax_sig * 2.0 ** e).astype(np.float32)
+    y[0, 3] = amax_sig * 2.0 ** e
+    return _bits(y)
+
+
+def pin_mxfp4_shared_exponent_closed_form(o):
+    """A block whose absmax is m * 2^e (1 <= m < 2) has scale code e - 2 + 127; its
+    absmax element becomes 4 (m < 1.25 by RNE, ...) up to 6, and the dequantised
+    absmax m * 2^e is met to within half an E2M1 step."""
+    for m, code_max in ((1.0, 0x6), (1.25, 0x6), (1.5, 0x7), (1.75, 0x7), (1.2, 0x6), (1.3, 0x7)):
+        for e in (-20, -3, 0, 5, 60):
+            y = _mx_block_y(m, e, 32, seed=e + 100)
+            q, sc = o.mxfp4(y)
+            assert sc[0, 0] == e - 2 + 127, (m, e, sc[0, 0])
+            c = (q[0, 1] >> 4) & 0xF        # element 3 is the high nibble of byte 1
+            assert c == code_max, (m, e, hex(c))
+
+
+def pin_mxfp4_all_zero_block(o):
+    y = np.zeros((1, 64), np.uint16)
+    y[0, 40] = _bits(np.array([0.75]))[0]
+    q, sc = o.mxfp4(y)
+    assert sc[0, 0] == 0 and np.all(q[0, :16] == 0)
+    assert sc[0, 1] == -1 - 2 + 127 and ((q[0, 20] & 0xF) == 0x7)   # 0.75 / 2^-3 = 6
+
+
+def pin_mxfp4_bruteforce(o):
+    """Exact shared exponent and exhaustive-search codes on random blocks."""
+    rng = np.random.default_rng(52)
+    y = (rng.standard_normal((2, 128)) * np.exp2(rng.uniform(-8, 8, (2, 1)))).astype(np.float32)
+    yb = _bits(y)
+    q, sc = o.mxfp4(yb)
+    bq, bsc = bf.mxfp4(yb)
+    assert np.array_equal(sc, bsc) and np.array_equal(q, bq)
+
+
+def pin_mxfp4_error_bound(o):
+    """|dequant - y| <= half an E2M1 step at that magnitude, times the scale."""
+    y = _random_y(3, 256, 53)
+    q, sc = o.mxfp4(y)
+    yf = bf16_bits_to_f32(y).astype(np.float64).reshape(3, 8, 32)
+    X = np.exp2(sc.astype(np.float64) - 127)[:, :, None]
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(3, 256)
+    dq = np.vectorize(o.e2m1_to_double)(codes).reshape(3, 8, 32) * X
+    v = np.abs(yf / X)
+    step = np.where(v < 1, 0.5, np.where(v < 2, 0.5, np.where(v < 4, 1.0, 2.0)))
+    assert np.all(np.abs(dq - yf) <= np.maximum(step / 2 * X, np.where(v > 6, (v - 6) * X, 0)) + 1e-300)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -40,6 +40,11 @@ MUTANTS = {
     "e4m3_subnormal_scale": [("ldexp((double)m, -6 - 3)", "ldexp((double)m, -6 - 2)")],
     "e4m3_no_saturation": [("if (r > 448.0) r = 448.0;", "")],
     "norm_without_square": [("ss += x * x;", "ss += fabs(x);")],
+    "mx_emax_off_by_one": [("shared_exp = (ex - 1) - 2;", "shared_exp = (ex - 1) - 1;")],
+    "mx_floor_log2_off": [("shared_exp = (ex - 1) - 2;", "shared_exp = ex - 2;")],
+    "e2m1_no_saturation": [("if (r > 6.0) r = 6.0;", "")],
+    "e2m1_subnormal_wrong": [("if (r < 1.0) return sign | 0x1;", "if (r < 1.0) return sign;")],
+    "mx_nibble_order_swapped": [("qb[i] = (uint8_t)(lo | (hi << 4));", "qb[i] = (uint8_t)(hi | (lo << 4));")],
 }
 
 
