@@ -301,15 +301,21 @@ def measure_rows(frn, R, T, mode, seed, hbm, outlier=False, partial_std=0.5, H=H
         p, r, g = syn.make_inputs_device(R, T, H, seed=seed + k, partial_std=partial_std,
                                          outlier_frac=0.01 if outlier else 0.0)
         ro = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-        y = torch.empty_like(ro) if mode in ("norm", "quant_b") else None
-        q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device="cuda") if mode != "norm" else None
-        s = torch.empty((T, H // 128), dtype=torch.float32, device="cuda") if mode != "norm" else None
+        y = torch.empty_like(ro) if mode in ("norm", "quant_b", "mx_b") else None
+        if mode in ("mx_a", "mx_b"):
+            q = torch.empty((T, H // 2), dtype=torch.uint8, device="cuda")
+            s = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
+        else:
+            q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device="cuda") if mode != "norm" else None
+            s = torch.empty((T, H // 128), dtype=torch.float32, device="cuda") if mode != "norm" else None
         sets.append((p, r, g, ro, y, q, s))
 
     def body():
         for p, r, g, ro, y, q, s in sets:
             if mode == "norm":
                 frn.fused_reduce_rmsnorm(p, r, g, EPS, residual_out=ro, y=y)
+            elif mode in ("mx_a", "mx_b"):
+                frn.fused_reduce_rmsnorm_mxfp4(p, r, g, EPS, mode == "mx_b", residual_out=ro, y=y, q=q, scales=s)
             else:
                 frn.fused_reduce_rmsnorm_quant_per_group(p, r, g, EPS, 128, mode == "quant_b", residual_out=ro,
                                                          y=y, q=q, scales=s)
@@ -498,6 +504,7 @@ PROFILE_CASES = {
     "prefill_quant_a": (2, 8192, H, "quant_a", True, 1.0),
     "prefill_quant_b": (2, 8192, H, "quant_b", True, 1.0),
     "quant_R4_T32": (4, 32, 4096, "quant_b", False, 0.5),
+    "prefill_mx_a": (2, 8192, H, "mx_a", True, 1.0),
 }
 
 
@@ -508,18 +515,25 @@ def run_profile_case(name: str, iters: int):
     R, T, Hh, mode, outlier, std = PROFILE_CASES[name]
     p, r, g = syn.make_inputs_device(R, T, Hh, seed=4242, partial_std=std, outlier_frac=0.01 if outlier else 0.0)
     ro = torch.empty((T, Hh), dtype=torch.bfloat16, device="cuda")
-    y = torch.empty_like(ro) if mode != "quant_a" else None
-    q = torch.empty((T, Hh), dtype=torch.float8_e4m3fn, device="cuda") if mode != "norm" else None
-    s = torch.empty((T, Hh // 128), dtype=torch.float32, device="cuda") if mode != "norm" else None
+    y = torch.empty_like(ro) if mode not in ("quant_a", "mx_a") else None
+    if mode.startswith("mx"):
+        q = torch.empty((T, Hh // 2), dtype=torch.uint8, device="cuda")
+        s = torch.empty((T, Hh // 32), dtype=torch.uint8, device="cuda")
+    else:
+        q = torch.empty((T, Hh), dtype=torch.float8_e4m3fn, device="cuda") if mode != "norm" else None
+        s = torch.empty((T, Hh // 128), dtype=torch.float32, device="cuda") if mode != "norm" else None
     for _ in range(2 + iters):
         if mode == "norm":
             frn.fused_reduce_rmsnorm(p, r, g, EPS, residual_out=ro, y=y)
+        elif mode.startswith("mx"):
+            frn.fused_reduce_rmsnorm_mxfp4(p, r, g, EPS, mode == "mx_b", residual_out=ro, y=y, q=q, scales=s)
         else:
             frn.fused_reduce_rmsnorm_quant_per_group(p, r, g, EPS, 128, mode == "quant_b", residual_out=ro, y=y, q=q,
                                                      scales=s)
     torch.cuda.synchronize()
     print(json.dumps({"case": name, "R": R, "T": T, "H": Hh, "mode": mode, "iters": iters,
-                      "launch": frn.query_launch(T, Hh, R, mode != "norm"),
+                      "launch": frn.query_launch(T, Hh, R, {"norm": 0, "quant_a": 1, "quant_b": 2, "mx_a": 3,
+                                                            "mx_b": 4}[mode]),
                       "bytes_per_call": syn.algorithmic_bytes(R, T, Hh, mode)}))
 
 
@@ -597,13 +611,15 @@ def main():
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(ach / hbm, 4), "traffic": recorded_traffic("decode64"),
                     "algorithmic_bytes": b64, "kernel_sources": kernel_source_hash(),
-                    "kernel": "frn_row_kernel<8, norm, cluster> at T=64 (the step's largest call)",
+                    "kernel": "frn_row_kernel<8, norm> at T=64, one 896-thread CTA per row (the step's largest call)",
                     "peak_kind": peak_kind}
         large = [measure_rows(frn, 8, syn.sweep_tokens(m), "norm", 20000 + i, hbm)
                  for i, m in enumerate((16 << 20, 32 << 20, 64 << 20))]
         large.append(measure_rows(frn, 2, 8192, "quant_a", 30000, hbm, outlier=True, partial_std=1.0))
         large.append(measure_rows(frn, 2, 8192, "quant_b", 31000, hbm, outlier=True, partial_std=1.0))
         large.append(measure_rows(frn, 2, 8192, "norm", 32000, hbm, outlier=True, partial_std=1.0))
+        large.append(measure_rows(frn, 2, 8192, "mx_a", 33000, hbm, outlier=True, partial_std=1.0))
+        large.append(measure_rows(frn, 2, 8192, "mx_b", 34000, hbm, outlier=True, partial_std=1.0))
         extras["large_T"] = large
         extras["sweep"] = [dict(msg_bytes=m, **measure_rows(frn, 8, syn.sweep_tokens(m), "norm", 40000 + i, hbm))
                            for i, m in enumerate(syn.SWEEP_BYTES)]

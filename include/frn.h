@@ -131,6 +131,28 @@ frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* partials, int
                                                 frn_stream_t stream);
 
 /*
+ * As fused_reduce_rmsnorm, then MXFP4 of y -- the third fused output variant
+ * ("Fix: add missing end_sync barrier in fused allreduce+rmsnorm kernel", AITER
+ * PR 4346, Pull request overview: the MXFP4 1-stage variant).  The pages give
+ * no format; this follows the OCP Microscaling Formats (MX) v1.0 conversion:
+ *   blocks of 32 consecutive elements of y along H;
+ *   shared_exp = floor(log2(max |y| over the block)) - 2 (the emax of E2M1),
+ *     clamped to [-127, 127];  scale code = shared_exp + 127 (E8M0);
+ *   element = E2M1 round-to-nearest-even, saturating to +-6, of y / 2^shared_exp;
+ *   an all-zero block gets scale code 0 and zero elements.
+ *
+ *   y             NULL -> (fp4, scale) + residual_out;  bf16 [T, H] -> (bf16, fp4, scale)
+ *   q_fp4         uint8 [T, H/2]: element 2i in the low nibble of byte i (16-byte aligned)
+ *   scales_e8m0   uint8 [T, H/32]
+ *   H % 32 == 0; other arguments, conventions and errors as for fused_reduce_rmsnorm.
+ */
+frn_status fused_reduce_rmsnorm_mxfp4(const void* const* partials, int R,
+                                      const void* residual, const void* gamma,
+                                      void* residual_out, void* y,
+                                      void* q_fp4, void* scales_e8m0,
+                                      int64_t T, int H, float eps, frn_stream_t stream);
+
+/*
  * The adjacent steps of the same layer, on the same kernels ("ROCm AITER fused
  * all-reduce + RMSNorm", vLLM PR 37646 summary, implementation breakdown item
  * 2: the rms_norm and fused_add_rms_norm patterns).
@@ -251,7 +273,9 @@ frn_status frn_set_stream_groups(int groups);
 /*
  * Report the launch a call with these sizes would use on the current device:
  * kernel (1 row, 2 stream), CTAs per row (cluster size; 1 for the stream
- * kernel), threads per CTA, and CTAs in the grid.  Output pointers may be NULL.
+ * kernel and for a single wide CTA), threads per CTA, and CTAs in the grid.
+ * quant: 0 no quant, 1 / 2 per-group FP8 without / with y, 3 / 4 MXFP4
+ * without / with y.  Output pointers may be NULL.
  */
 frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int* ctas_per_row,
                             int* threads_per_cta, int64_t* grid_ctas);

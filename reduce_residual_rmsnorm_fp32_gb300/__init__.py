@@ -32,7 +32,7 @@ __all__ = [
     "FrnError", "fused_reduce_rmsnorm", "fused_reduce_rmsnorm_quant_per_group", "library",
     "set_pdl", "set_kernel", "set_ctas_per_row", "set_stream_groups", "query_launch", "device_status", "set_test_hooks",
     "status_string", "version", "KERNEL_AUTO", "KERNEL_ROWS", "KERNEL_STREAM",
-    "fused_add_rmsnorm", "rmsnorm", "unfused_workspace_bytes", "unfused_reduce_rmsnorm", "unfused_reduce_rmsnorm_noalloc",
+    "fused_reduce_rmsnorm_mxfp4", "fused_add_rmsnorm", "rmsnorm", "unfused_workspace_bytes", "unfused_reduce_rmsnorm", "unfused_reduce_rmsnorm_noalloc",
     "STATIC_WORKSPACE_BYTES",
     "FRN_OK", "FRN_ERR_INVALID_ARG", "FRN_ERR_UNSUPPORTED", "FRN_ERR_MISALIGNED", "FRN_ERR_CUDA",
     "FRN_ERR_TIMEOUT", "MAX_PARTIALS", "MAX_HIDDEN", "QUANT_GROUP",
@@ -85,6 +85,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_device_status.restype = i32
     lib.frn_set_test_hooks.argtypes = [i32, i64]
     lib.frn_set_test_hooks.restype = i32
+    lib.fused_reduce_rmsnorm_mxfp4.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, vp, vp, i64, i32, f32, vp]
+    lib.fused_reduce_rmsnorm_mxfp4.restype = i32
     lib.frn_fused_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i32, f32, vp]
     lib.frn_fused_add_rmsnorm.restype = i32
     lib.frn_rmsnorm.argtypes = [vp, vp, vp, i64, i32, f32, vp]
@@ -145,10 +147,11 @@ def set_stream_groups(groups: int) -> None:
     _check(library().frn_set_stream_groups(int(groups)))
 
 
-def query_launch(T: int, H: int, R: int, quant: bool = False) -> tuple[int, int, int, int]:
-    """(kernel, ctas_per_row, threads_per_cta, grid_ctas) a call would use on the current device."""
+def query_launch(T: int, H: int, R: int, quant: int = 0) -> tuple[int, int, int, int]:
+    """(kernel, ctas_per_row, threads_per_cta, grid_ctas) a call would use on the current device.
+    quant: 0 none, 1 / 2 FP8 without / with y, 3 / 4 MXFP4 without / with y."""
     k, c, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
-    _check(library().frn_query_launch(int(T), int(H), int(R), int(bool(quant)), ctypes.byref(k), ctypes.byref(c),
+    _check(library().frn_query_launch(int(T), int(H), int(R), int(quant), ctypes.byref(k), ctypes.byref(c),
                                       ctypes.byref(t), ctypes.byref(g)))
     return k.value, c.value, t.value, g.value
 
@@ -368,3 +371,39 @@ def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, *, y: torch
         st = library().frn_rmsnorm(_ptr(x), _ptr(gamma), _ptr(y), T, H, float(eps), _stream(stream, dev))
     _check(st)
     return y
+
+
+def fused_reduce_rmsnorm_mxfp4(partials, residual: torch.Tensor | None, gamma: torch.Tensor, eps: float = 1e-6,
+                               emit_bf16: bool = False, *, residual_out: torch.Tensor | None = None,
+                               y: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                               scales: torch.Tensor | None = None, stream=None):
+    """Fused epilogue with MXFP4 output (OCP MX: 32-blocks, E8M0 scale, E2M1).
+
+    Returns ``((q, scales), residual_out)`` or, with ``emit_bf16``,
+    ``((y, q, scales), residual_out)``; ``q`` is uint8 ``[T, H/2]`` (element 2i in
+    the low nibble), ``scales`` uint8 ``[T, H/32]`` E8M0 codes."""
+    ptrs, R, T, H, dev = _partials(partials)
+    if residual is not None:
+        _check_tensor(residual, "residual", torch.bfloat16, (T, H), dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
+    if H % 32:
+        raise ValueError(f"H={H} must be a multiple of 32")
+    emit_bf16 = emit_bf16 or y is not None
+    residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if residual_out is None else residual_out
+    if emit_bf16 and y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    q = torch.empty((T, H // 2), dtype=torch.uint8, device=dev) if q is None else q
+    scales = torch.empty((T, H // 32), dtype=torch.uint8, device=dev) if scales is None else scales
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
+    if y is not None:
+        _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
+    _check_tensor(q, "q", torch.uint8, (T, H // 2), dev)
+    _check_tensor(scales, "scales", torch.uint8, (T, H // 32), dev)
+    arr = (ctypes.c_void_p * R)(*ptrs)
+    with torch.cuda.device(dev):
+        st = library().fused_reduce_rmsnorm_mxfp4(arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y),
+                                                  _ptr(q), _ptr(scales), T, H, float(eps), _stream(stream, dev))
+    _check(st)
+    if emit_bf16:
+        return (y, q, scales), residual_out
+    return (q, scales), residual_out

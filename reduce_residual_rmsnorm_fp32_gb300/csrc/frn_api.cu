@@ -92,8 +92,19 @@ frn_status status_word(unsigned int** out) {
 }
 
 // Launch shape of the row kernel.  A row's ntiles warp tiles go to C CTAs of
-// a cluster.  The results do not depend on this choice (the reduction tree is
-// fixed by H).
+// a cluster, or (wide) to one CTA of up to 1024 threads.  The results do not
+// depend on this choice (the reduction tree is fixed by H).
+frn::RowPlan wide_plan(long long T, int ntiles) {
+    frn::RowPlan plan;
+    plan.ctas_per_row = 1;
+    plan.tiles_per_cta = ntiles;
+    plan.threads = ntiles * 32;
+    plan.grid = T;
+    return plan;
+}
+
+bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
+
 frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     const int nvec = H / frn::kVecElems;
     const int ntiles = ceil_div(nvec, frn::kTileVecs);
@@ -101,15 +112,11 @@ frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     const int cmax = ntiles < 8 ? ntiles : 8;
     int C;
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
-    if (forced == 1 && ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8) {
-        // one wide CTA (up to 1024 threads) per row, no cluster
-        frn::RowPlan plan;
-        plan.ctas_per_row = 1;
-        plan.tiles_per_cta = ntiles;
-        plan.threads = ntiles * 32;
-        plan.grid = T;
-        return plan;
-    }
+    if (forced == 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
+    // From 40 rows on, a row wider than one 512-thread CTA goes to a single wide
+    // CTA: with that many rows the GPU is busy anyway, and the cluster launch
+    // and its barriers cost more than the extra SMs per row gain.
+    if (forced == 0 && cmin > 1 && T >= 40 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
     if (forced > 0) {
         C = forced < cmin ? cmin : (forced > cmax ? cmax : forced);
     } else if (cmin == 1) {
@@ -161,14 +168,24 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
     return plan;
 }
 
-// Which kernel: a row that fits one CTA (H <= 4096) streams best through the
-// row kernel at any T (several CTAs, i.e. rows, in flight per SM); a wider row
-// goes to the stream kernel once there is a row per SM.
-int choose_kind(long long T, int H, int num_sms) {
+// Which kernel (measured on GB300 at H = 7168, R = 1..8, T = 8..8192):
+//  * a row that fits one 512-thread CTA (H <= 4096): the row kernel at any T
+//    (several rows in flight per SM);
+//  * a row for a wide CTA (H <= 8192, R <= 8): the row kernel, except from
+//    2 rows per SM on where the stream kernel's overlap of one row's epilogue
+//    with the next rows' loads wins -- R >= 4, R == 1, or a variant that writes
+//    y and a quant (B) from 8 rows per SM on;
+//  * a wider row: the stream kernel from one row per SM on.
+int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     const int forced = g_force_kernel.load(std::memory_order_relaxed);
     if (forced == kRows || forced == kStream) return forced;
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
     if (ntiles <= frn::kMaxTilesPerCta) return kRows;
+    if (wide_possible(ntiles, R)) {
+        if (T < 2LL * num_sms) return kRows;
+        const bool heavy_b = (quant == 2 || quant == 4) && T >= 8LL * num_sms;
+        return (R >= 4 || R == 1 || heavy_b) ? kStream : kRows;
+    }
     return T >= num_sms ? kStream : kRows;
 }
 
@@ -206,7 +223,10 @@ struct Call {
     long long workspace_bytes;
     long long workspace_needed;
     bool no_residual_out;   // plain RMSNorm: residual_out is not written
+    void* mx_scales;        // MXFP4 (quant 3, 4): E8M0 codes; q holds the packed E2M1 codes
 };
+
+bool is_mx(int quant) { return quant >= 3; }
 
 // Everything that can be checked on the host: scalars, pointers, alignment,
 // overlap.  Returns FRN_OK with *empty set when T == 0 (nothing to launch).
@@ -221,7 +241,9 @@ frn_status validate(const Call& c, bool* empty) {
     if (H % 8 != 0 || H > FRN_MAX_HIDDEN)
         return fail(FRN_ERR_UNSUPPORTED, "H=%d must be a multiple of 8 and <= %d", H, FRN_MAX_HIDDEN);
     if (!std::isfinite(c.eps) || c.eps < 0.0f) return fail(FRN_ERR_INVALID_ARG, "eps must be finite and >= 0");
-    if (c.quant) {
+    if (is_mx(c.quant)) {
+        if (H % 32 != 0) return fail(FRN_ERR_UNSUPPORTED, "H=%d: MXFP4 needs a multiple of 32", H);
+    } else if (c.quant) {
         if (c.group_size < 1 || H % c.group_size != 0)
             return fail(FRN_ERR_INVALID_ARG, "group_size=%d must divide H=%d", c.group_size, H);
         if (c.group_size != FRN_QUANT_GROUP)
@@ -239,15 +261,17 @@ frn_status validate(const Call& c, bool* empty) {
     }
     if (!c.gamma) return fail(FRN_ERR_INVALID_ARG, "gamma is NULL");
     if (!c.residual_out && !c.no_residual_out) return fail(FRN_ERR_INVALID_ARG, "residual_out is NULL");
-    if (c.quant != 1 && !c.y) return fail(FRN_ERR_INVALID_ARG, "y is NULL");
-    if (c.quant && (!c.q || !c.scales)) return fail(FRN_ERR_INVALID_ARG, "q / scales is NULL");
+    if (!c.y && !(c.quant == 1 || c.quant == 3)) return fail(FRN_ERR_INVALID_ARG, "y is NULL");
+    if (c.quant && !is_mx(c.quant) && (!c.q || !c.scales)) return fail(FRN_ERR_INVALID_ARG, "q / scales is NULL");
+    if (is_mx(c.quant) && (!c.q || !c.mx_scales)) return fail(FRN_ERR_INVALID_ARG, "q_fp4 / scales is NULL");
     if (!aligned(c.gamma, 16)) return fail(FRN_ERR_MISALIGNED, "gamma not 16-byte aligned");
     if (c.residual && !aligned(c.residual, 16)) return fail(FRN_ERR_MISALIGNED, "residual not 16-byte aligned");
     if (c.residual_out && !aligned(c.residual_out, 16))
         return fail(FRN_ERR_MISALIGNED, "residual_out not 16-byte aligned");
     if (c.y && !aligned(c.y, 16)) return fail(FRN_ERR_MISALIGNED, "y not 16-byte aligned");
     if (c.quant && !aligned(c.q, 16)) return fail(FRN_ERR_MISALIGNED, "q not 16-byte aligned");
-    if (c.quant && !aligned(c.scales, 4)) return fail(FRN_ERR_MISALIGNED, "scales not 4-byte aligned");
+    if (c.quant && !is_mx(c.quant) && !aligned(c.scales, 4))
+        return fail(FRN_ERR_MISALIGNED, "scales not 4-byte aligned");
     if (T > (1LL << 40) / H) return fail(FRN_ERR_UNSUPPORTED, "T*H too large");
     if (c.workspace_needed > 0) {
         if (!c.workspace) return fail(FRN_ERR_INVALID_ARG, "workspace is NULL (%lld bytes needed)", c.workspace_needed);
@@ -264,7 +288,10 @@ frn_status validate(const Call& c, bool* empty) {
     int nout = 0;
     if (c.residual_out) outs[nout++] = range_of(c.residual_out, act, "residual_out");
     if (c.y) outs[nout++] = range_of(c.y, act, "y");
-    if (c.quant) {
+    if (is_mx(c.quant)) {
+        outs[nout++] = range_of(c.q, T * static_cast<long long>(H) / 2, "q_fp4");
+        outs[nout++] = range_of(c.mx_scales, T * static_cast<long long>(H) / 32, "scales_e8m0");
+    } else if (c.quant) {
         outs[nout++] = range_of(c.q, T * static_cast<long long>(H), "q");
         outs[nout++] = range_of(c.scales, 4LL * T * (H / c.group_size), "scales");
     }
@@ -297,8 +324,13 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
     p.gamma = static_cast<const uint4*>(c.gamma);
     p.residual_out = static_cast<uint4*>(c.residual_out);
     p.y = static_cast<uint4*>(c.y);
-    p.q = static_cast<uint2*>(c.q);
-    p.scales = c.scales;
+    if (is_mx(c.quant)) {
+        p.q4 = static_cast<uint32_t*>(c.q);
+        p.mx_scales = static_cast<uint8_t*>(c.mx_scales);
+    } else {
+        p.q = static_cast<uint2*>(c.q);
+        p.scales = c.scales;
+    }
     p.T = c.T;
     p.R = c.R;
     p.H = c.H;
@@ -322,7 +354,7 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // The fused epilogue (one kernel).  quant as in Call; the kernel writes c.y
 // when it is not NULL.
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
-    const int kind = choose_kind(c.T, c.H, sms);
+    const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
     const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
@@ -340,13 +372,17 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
         switch (quant) {
             case 0: e = frn::launch_stream_norm(p, splan, s, pdl); break;
             case 1: e = frn::launch_stream_quant_a(p, splan, s, pdl); break;
-            default: e = frn::launch_stream_quant_b(p, splan, s, pdl); break;
+            case 2: e = frn::launch_stream_quant_b(p, splan, s, pdl); break;
+            case 3: e = frn::launch_stream_mx_a(p, splan, s, pdl); break;
+            default: e = frn::launch_stream_mx_b(p, splan, s, pdl); break;
         }
     } else {
         switch (quant) {
             case 0: e = frn::launch_rows_norm(p, rplan, s, pdl); break;
             case 1: e = frn::launch_rows_quant_a(p, rplan, s, pdl); break;
-            default: e = frn::launch_rows_quant_b(p, rplan, s, pdl); break;
+            case 2: e = frn::launch_rows_quant_b(p, rplan, s, pdl); break;
+            case 3: e = frn::launch_rows_mx_a(p, rplan, s, pdl); break;
+            default: e = frn::launch_rows_mx_b(p, rplan, s, pdl); break;
         }
     }
     if (e != cudaSuccess) return fail(FRN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
@@ -425,6 +461,15 @@ FRN_EXPORT frn_status fused_reduce_rmsnorm_quant_per_group(const void* const* pa
                                                            int group_size, frn_stream_t stream) {
     const Call c{partials, R, residual, gamma, residual_out, y, q_e4m3, scales, T, H, eps, group_size,
                  y ? 2 : 1, nullptr, 0, 0, false};
+    return run(c, stream);
+}
+
+FRN_EXPORT frn_status fused_reduce_rmsnorm_mxfp4(const void* const* partials, int R, const void* residual,
+                                                 const void* gamma, void* residual_out, void* y, void* q_fp4,
+                                                 void* scales_e8m0, int64_t T, int H, float eps,
+                                                 frn_stream_t stream) {
+    const Call c{partials, R, residual, gamma, residual_out, y, q_fp4, nullptr, T, H, eps, 32, y ? 4 : 3,
+                 nullptr, 0, 0, false, scales_e8m0};
     return run(c, stream);
 }
 
@@ -588,13 +633,12 @@ FRN_EXPORT frn_status frn_device_status(int clear) {
 
 FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int* ctas_per_row,
                                        int* threads_per_cta, int64_t* grid_ctas) {
-    (void)quant;
-    if (R < 1 || T < 0 || H < 8 || H % 8 != 0 || H > FRN_MAX_HIDDEN)
+    if (R < 1 || T < 0 || H < 8 || H % 8 != 0 || H > FRN_MAX_HIDDEN || quant < 0 || quant > 4)
         return fail(FRN_ERR_INVALID_ARG, "bad sizes");
     int sms = 0;
     frn_status st = sm_count(&sms);
     if (st != FRN_OK) return st;
-    const int kind = choose_kind(T, H, sms);
+    const int kind = choose_kind(T, H, R, quant, sms);
     if (kernel) *kernel = kind;
     if (kind == kStream) {
         const frn::StreamPlan plan = choose_stream(T, H, R + 1, sms);

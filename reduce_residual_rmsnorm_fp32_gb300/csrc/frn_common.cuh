@@ -41,7 +41,13 @@ constexpr int kMaxTiles = 64;       // H <= 16384 (two tile slots per lane)
 constexpr int kMaxThreads = kMaxTilesPerCta * 32;
 constexpr int kGroup = 128;         // quant group (elements)
 
-enum Mode : int { kNorm = 0, kQuantA = 1, kQuantB = 2 };
+// Output variants: norm only; per-group-128 e4m3 without (A) / with (B) the
+// bf16 y; MXFP4 (32-blocks, E8M0 scale, E2M1) without (A) / with (B) y.
+enum Mode : int { kNorm = 0, kQuantA = 1, kQuantB = 2, kMxA = 3, kMxB = 4 };
+
+__host__ __device__ constexpr bool mode_writes_y(int m) { return m == kNorm || m == kQuantB || m == kMxB; }
+__host__ __device__ constexpr bool mode_fp8(int m) { return m == kQuantA || m == kQuantB; }
+__host__ __device__ constexpr bool mode_mx(int m) { return m == kMxA || m == kMxB; }
 
 struct Params {
     const uint4* partials[kMaxPartials];
@@ -51,6 +57,8 @@ struct Params {
     uint4* y;                // bf16 output (kNorm, kQuantB)
     uint2* q;                // e4m3 codes, 8 per vector (kQuantA, kQuantB)
     float* scales;           // [T, H/128]
+    uint32_t* q4;            // MXFP4: 8 E2M1 codes per vector, element 2i in the low nibble
+    uint8_t* mx_scales;      // MXFP4: E8M0 codes [T, H/32]
     long long T;
     int R;
     int H;
@@ -365,6 +373,50 @@ __device__ __forceinline__ void quant8(const uint4 yb, uint2& qq, float& sc) {
         for (int i = 0; i < 4; ++i) c[i] = pack_e4m3x2(qv[2 * i], qv[2 * i + 1]);
         qq.x = c[0] | (c[1] << 16);
         qq.y = c[2] | (c[3] << 16);
+    }
+}
+
+// OCP Microscaling (MX v1.0) FP4: E2M1, round to nearest even, saturating to
+// +-6; the low nibble of the result holds the second source operand.
+__device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// MXFP4 of one bf16 y vector: a block of 32 elements is an aligned group of 4
+// lanes, and all 32 lanes must call this.  shared_exp = floor(log2(absmax)) - 2
+// (2 = emax of E2M1), clamped to [-127, 127]; elements y * 2^-shared_exp (exact)
+// rounded to E2M1.  An all-zero block gives scale code 0 and zero elements.
+__device__ __forceinline__ void mxfp4_8(const uint4 yb, uint32_t& packed, uint32_t& code) {
+    uint32_t mp = absmax_bf16x2(0u, yb.x);
+    mp = absmax_bf16x2(mp, yb.y);
+    mp = absmax_bf16x2(mp, yb.z);
+    mp = absmax_bf16x2(mp, yb.w);
+    float amax = fmaxf(__uint_as_float(mp << 16), __uint_as_float(mp & 0xFFFF0000u));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    packed = 0u;
+    code = 0u;
+    if (amax > 0.0f) {
+        const uint32_t bits = __float_as_uint(amax);
+        const int ef = static_cast<int>((bits >> 23) & 0xFFu);
+        // floor(log2(amax)): the exponent field, or for an fp32 subnormal the
+        // position of the leading mantissa bit (value = m * 2^-149)
+        const int lg = ef != 0 ? ef - 127 : (31 - __clz(static_cast<int>(bits & 0x7FFFFFu))) - 149;
+        int shared = lg - 2;
+        shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
+        code = static_cast<uint32_t>(shared + 127);
+        const float inv = __int_as_float((127 - shared) << 23);   // 2^-shared; shared <= 125 for bf16 y
+        float v[8];
+        unpack8(yb, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], inv);
+        packed = pack_e2m1x2(v[0], v[1]) | (pack_e2m1x2(v[2], v[3]) << 8) | (pack_e2m1x2(v[4], v[5]) << 16) |
+                 (pack_e2m1x2(v[6], v[7]) << 24);
     }
 }
 

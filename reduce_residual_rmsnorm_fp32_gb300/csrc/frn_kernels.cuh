@@ -23,6 +23,10 @@ cudaError_t launch_rows_quant_b(const Params& p, const RowPlan& plan, cudaStream
 cudaError_t launch_stream_norm(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl);
 cudaError_t launch_stream_quant_a(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl);
 cudaError_t launch_stream_quant_b(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl);
+cudaError_t launch_rows_mx_a(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl);
+cudaError_t launch_rows_mx_b(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl);
+cudaError_t launch_stream_mx_a(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl);
+cudaError_t launch_stream_mx_b(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl);
 
 // The unfused comparison stages (frn_launch_unfused.cu).
 cudaError_t launch_reduce(const Params& p, float4* xsum, int num_sms, cudaStream_t stream, bool pdl);

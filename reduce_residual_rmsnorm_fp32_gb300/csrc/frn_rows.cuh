@@ -87,16 +87,24 @@ __global__ void __launch_bounds__(MAXT) frn_row_kernel(const __grid_constant__ P
     }
     if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
     const uint4 yb = rms_y(ro, rstd, g);
-    if constexpr (MODE != kQuantA) {
+    if constexpr (mode_writes_y(MODE)) {
         if (valid) p.y[off] = yb;
     }
-    if constexpr (MODE != kNorm) {
+    if constexpr (mode_fp8(MODE)) {
         uint2 qq;
         float sc;
         quant8(yb, qq, sc);
         if (valid) {
             p.q[off] = qq;
             if ((lane & 15) == 0) p.scales[row * (p.H / kGroup) + (j >> 4)] = sc;
+        }
+    }
+    if constexpr (mode_mx(MODE)) {
+        uint32_t packed, code;
+        mxfp4_8(yb, packed, code);
+        if (valid) {
+            p.q4[off] = packed;
+            if ((lane & 3) == 0) p.mx_scales[row * (p.H / 32) + (j >> 2)] = static_cast<uint8_t>(code);
         }
     }
 

@@ -222,16 +222,24 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
         for (int t = 0; t < TPW; ++t) {
             const uint4 gt = kGammaInRegs ? g[kGammaInRegs ? t : 0] : ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
             const uint4 yb = rms_y(rov[t], rstd, gt);
-            if constexpr (MODE != kQuantA) {
+            if constexpr (mode_writes_y(MODE)) {
                 if (vt[t]) p.y[rbase + jt[t]] = yb;
             }
-            if constexpr (MODE != kNorm) {
+            if constexpr (mode_fp8(MODE)) {
                 uint2 qq;
                 float sc;
                 quant8(yb, qq, sc);
                 if (vt[t]) {
                     p.q[rbase + jt[t]] = qq;
                     if ((lane & 15) == 0) p.scales[row * ng + (jt[t] >> 4)] = sc;
+                }
+            }
+            if constexpr (mode_mx(MODE)) {
+                uint32_t packed, code;
+                mxfp4_8(yb, packed, code);
+                if (vt[t]) {
+                    p.q4[rbase + jt[t]] = packed;
+                    if ((lane & 3) == 0) p.mx_scales[row * (p.H / 32) + (jt[t] >> 2)] = static_cast<uint8_t>(code);
                 }
             }
         }

@@ -126,7 +126,8 @@ def algorithmic_bytes(R: int, T: int, H: int, mode: str = "norm", group_size: in
     """Bytes a perfect kernel moves through HBM per call.
 
     mode: "norm" (residual_out + y), "quant_a" (residual_out + fp8 + scales),
-    "quant_b" (residual_out + y + fp8 + scales).
+    "quant_b" (residual_out + y + fp8 + scales), "mx_a" (residual_out + packed
+    fp4 + E8M0 scales per 32), "mx_b" (the same + y).
     """
     n = T * H
     b = 2 * n * R + 2 * H + 2 * n          # partials + gamma + residual_out
@@ -138,6 +139,10 @@ def algorithmic_bytes(R: int, T: int, H: int, mode: str = "norm", group_size: in
         b += n + 4 * (n // group_size)
     elif mode == "quant_b":
         b += 3 * n + 4 * (n // group_size)
+    elif mode == "mx_a":
+        b += n // 2 + n // 32
+    elif mode == "mx_b":
+        b += 2 * n + n // 2 + n // 32
     else:
         raise ValueError(mode)
     return b

@@ -1,0 +1,96 @@
+"""MXFP4 output variant (OCP MX: 32-element blocks, E8M0 scale, E2M1 elements)
+against the oracle, under both kernels and both output variants.
+
+Matching rule: residual_out bit-exact, y within one bf16 ulp; in every block
+whose y equals the oracle's bit for bit, the E8M0 code and all E2M1 codes are
+equal; elsewhere (a 1-ulp y flip) E2M1 codes differ by at most one step, on at
+most 0.1% of all elements."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reduce_residual_rmsnorm_fp32_gb300 as frn
+from reduce_residual_rmsnorm_fp32_gb300 import synthetic as syn
+from frn_testlib import DevInputs, assert_residual_exact, assert_y_close, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes(q):
+    T, Hh = q.shape
+    return np.stack([q & 0xF, q >> 4], axis=-1).reshape(T, 2 * Hh)
+
+
+def _ordered_e2m1(c):
+    c = c.astype(np.int32)
+    return np.where(c & 0x8, -(c & 0x7), c & 0x7)
+
+
+def check_mx(inp, what, rows=None):
+    d = DevInputs(inp)
+    (qa, sa), roa = frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps)
+    (y, qb, sb), rob = frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps, emit_bf16=True)
+    yn, ron = frn.fused_reduce_rmsnorm(d.partials, d.residual, d.gamma, inp.eps)
+    torch.cuda.synchronize()
+    assert torch.equal(qa, qb) and torch.equal(sa, sb) and torch.equal(roa, rob) and torch.equal(roa, ron)
+    assert torch.equal(y, yn)
+    ro, yb, q, s = host_bits(rob), host_bits(y), host_bits(qb), host_bits(sb)
+    sub = inp
+    if rows is not None:
+        sub = syn.Inputs(inp.partials[:, rows], inp.residual[rows], inp.gamma, inp.eps)
+        ro, yb, q, s = ro[rows], yb[rows], q[rows], s[rows]
+    rro, ry, rq, rs = oracle.Oracle().reduce_rmsnorm_mxfp4(sub.partials, sub.residual, sub.gamma, sub.eps, threads=8)
+    assert_residual_exact(ro, rro, what)
+    assert_y_close(yb, ry, what)
+    T, H = yb.shape
+    same = np.all(yb.reshape(T, H // 32, 32) == ry.reshape(T, H // 32, 32), axis=-1)
+    c, rc = _codes(q).reshape(T, H // 32, 32), _codes(rq).reshape(T, H // 32, 32)
+    assert np.array_equal(s[same], rs[same]), what
+    assert np.array_equal(c[same], rc[same]), what
+    dc = np.abs(_ordered_e2m1(c) - _ordered_e2m1(rc))
+    assert dc.max(initial=0) <= 1, what
+    assert (dc > 0).mean() <= 1e-3, what
+    return int((~same).sum())
+
+
+@pytest.fixture(params=[frn.KERNEL_ROWS, frn.KERNEL_STREAM], ids=["rows", "stream"])
+def kernel(request):
+    frn.set_kernel(request.param)
+    yield request.param
+    frn.set_kernel(frn.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("R,T,H", [(2, 4, 256), (8, 64, 7168), (4, 32, 4096), (3, 17, 1024), (1, 5, 32),
+                                   (16, 3, 16384), (2, 300, 7168)])
+def test_mxfp4_parity(R, T, H, kernel):
+    check_mx(syn.make_inputs(R, T, H, seed=R + T + H, partial_std=0.5), f"mx R={R} T={T} H={H} k={kernel}")
+
+
+def test_mxfp4_prefill_outliers():
+    inp = syn.config_prefill(seed=4)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(inp.T, 40, replace=False), [0, inp.T - 1]]))
+    check_mx(inp, "mx prefill", rows=rows)
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -100, 2.0 ** -30, 2.0 ** 40])
+def test_mxfp4_magnitudes_and_zero_blocks(scale):
+    inp = syn.make_inputs(3, 6, 1024, seed=9)
+    f = syn.bf16_bits_to_f32(inp.partials) * np.float32(scale)
+    r = syn.bf16_bits_to_f32(inp.residual) * np.float32(scale)
+    p, res = syn.f32_to_bf16_bits(f), syn.f32_to_bf16_bits(r)
+    p[:, 2, 64:96] = 0
+    res[2, 64:96] = 0
+    inp = syn.Inputs(p, res, inp.gamma, 1e-30)
+    check_mx(inp, f"mx scale {scale}")
+    d = DevInputs(inp)
+    (q, s), _ = frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps)
+    assert host_bits(s)[2, 2] == 0 and np.all(host_bits(q)[2, 32:48] == 0)
+
+
+def test_mxfp4_rejects_bad_h():
+    inp = syn.make_inputs(2, 2, 136, seed=1)
+    d = DevInputs(inp)
+    with pytest.raises(ValueError):
+        frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps)
