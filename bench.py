@@ -369,7 +369,10 @@ def measure_e2e(frn, steps: int):
     """The decode step through the public API from pinned host memory.  Every
     step copies all of its inputs (the four T values' partials and residuals,
     and gamma) host->device in one copy from one pinned buffer, makes the four
-    fused calls, and reads all outputs (residual_out and y) back in one copy."""
+    fused calls, and reads all outputs (residual_out and y) back in one copy.
+    Steps are pipelined the way a serving loop would run them: two device
+    buffer sets, the next step's host->device copy on its own stream while the
+    current step computes and its results are read back."""
     inps = [syn.config_decode(T, seed=500 + i) for i, T in enumerate(DECODE_T)]
     in_parts = []
     for inp in inps:
@@ -378,37 +381,57 @@ def measure_e2e(frn, steps: int):
     flat_in = np.concatenate(in_parts).view(np.int16)
     host_in = torch.from_numpy(flat_in).pin_memory()
     n_out = sum(2 * T * H for T in DECODE_T)
-    host_out = torch.empty((n_out,), dtype=torch.int16).pin_memory()
-    dev_in = torch.empty_like(host_in, device="cuda")
-    dev_out = torch.empty((n_out,), dtype=torch.int16, device="cuda")
-    # device views, in the order of the packed buffers
-    views, off, ooff = [], 0, 0
-    for T in DECODE_T:
-        npart, nres = R_DEC * T * H, T * H
-        p = dev_in[off:off + npart].view(torch.bfloat16).view(R_DEC, T, H)
-        r = dev_in[off + npart:off + npart + nres].view(torch.bfloat16).view(T, H)
-        off += npart + nres
-        ro = dev_out[ooff:ooff + T * H].view(torch.bfloat16).view(T, H)
-        y = dev_out[ooff + T * H:ooff + 2 * T * H].view(torch.bfloat16).view(T, H)
-        ooff += 2 * T * H
-        views.append((p, r, ro, y))
-    gamma_d = dev_in[off:off + H].view(torch.bfloat16)
+    host_out = [torch.empty((n_out,), dtype=torch.int16).pin_memory() for _ in range(2)]
+    dev_in = [torch.empty_like(host_in, device="cuda") for _ in range(2)]
+    dev_out = [torch.empty((n_out,), dtype=torch.int16, device="cuda") for _ in range(2)]
+
+    def views(di, do):
+        out, off, ooff = [], 0, 0
+        for T in DECODE_T:
+            npart, nres = R_DEC * T * H, T * H
+            p = di[off:off + npart].view(torch.bfloat16).view(R_DEC, T, H)
+            r = di[off + npart:off + npart + nres].view(torch.bfloat16).view(T, H)
+            off += npart + nres
+            ro = do[ooff:ooff + T * H].view(torch.bfloat16).view(T, H)
+            y = do[ooff + T * H:ooff + 2 * T * H].view(torch.bfloat16).view(T, H)
+            ooff += 2 * T * H
+            out.append((p, r, ro, y))
+        return out, di[off:off + H].view(torch.bfloat16)
+
+    vs = [views(dev_in[i], dev_out[i]) for i in range(2)]
     h2d = host_in.numel() * 2
-    d2h = host_out.numel() * 2
+    d2h = host_out[0].numel() * 2
+    compute = torch.cuda.current_stream()
+    copy_in = torch.cuda.Stream()
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
-    def one_step():
-        dev_in.copy_(host_in, non_blocking=True)
-        for p, r, ro, y in views:
-            frn.fused_reduce_rmsnorm(p, r, gamma_d, EPS, residual_out=ro, y=y)
-        host_out.copy_(dev_out, non_blocking=True)
+    def load(buf, k):
+        with torch.cuda.stream(copy_in):
+            if k >= 2:
+                copy_in.wait_event(consumed[buf])     # step k-2 has finished reading this buffer
+            dev_in[buf].copy_(host_in, non_blocking=True)
+            loaded[buf].record(copy_in)
 
-    for _ in range(3):
-        one_step()
+    def run(nsteps):
+        copy_in.wait_stream(compute)          # nothing of this run starts before the caller's last op
+        load(0, 0)
+        for k in range(nsteps):
+            b = k % 2
+            if k + 1 < nsteps:
+                load((k + 1) % 2, k + 1)
+            compute.wait_event(loaded[b])
+            calls, gamma_d = vs[b]
+            for p, r, ro, y in calls:
+                frn.fused_reduce_rmsnorm(p, r, gamma_d, EPS, residual_out=ro, y=y)
+            consumed[b].record(compute)
+            host_out[b].copy_(dev_out[b], non_blocking=True)
+
+    run(4)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(steps):
-        one_step()
+    run(steps)
     e1.record()
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3

@@ -257,9 +257,11 @@ int frn_version(void);
  *   1 forces the row kernel (one row per thread-block cluster, for few rows),
  *   2 forces the stream kernel (persistent, one CTA per SM, rows streamed
  *   through shared memory with TMA bulk copies, for many rows).
- * frn_set_ctas_per_row: row kernel only.  0 (default) chooses how many CTAs
- *   of a cluster share a row from T, H and the SM count; 1..8 forces it
- *   (rounded so that no CTA is empty).
+ * frn_set_ctas_per_row: row kernel only.  0 (default) chooses from T, H, R
+ *   and the SM count between one CTA per row and a cluster of CTAs per row;
+ *   1 forces one CTA per row (up to 1024 threads when H <= 8192 and R <= 8,
+ *   else the smallest cluster that holds the row); 2..8 force a cluster of
+ *   that many CTAs (rounded so that no CTA is empty).
  * frn_set_stream_groups: stream kernel only.  0 (default) chooses how many
  *   consumer groups (each taking every n-th row of a CTA, so that one group's
  *   epilogue overlaps the next group's loads) from H; 1..4 forces it, reduced
