@@ -283,10 +283,11 @@ frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int
                             int* threads_per_cta, int64_t* grid_ctas);
 
 /*
- * Device-side failure detection.  The stream kernel bounds every wait on its
- * shared-memory pipeline (default 2 s).  A wait that runs out makes the kernel
- * stop early and set a status word on the device; the call's outputs are then
- * incomplete.  frn_device_status reads that word for the current device --
+ * Device-side failure detection.  Every device-side wait is bounded (default
+ * 2 s): the stream kernel's shared-memory pipeline and the row kernel's wait
+ * for the tile sums of a row split over a cluster.  A wait that runs out sets a
+ * status word on the device and the kernel finishes without waiting further;
+ * the call's outputs are then incomplete.  frn_device_status reads that word for the current device --
  * synchronously, so call it after the work in question has completed (e.g.
  * after synchronising its stream) -- and returns FRN_ERR_TIMEOUT if it is set
  * (FRN_OK otherwise).  clear != 0 resets the word.

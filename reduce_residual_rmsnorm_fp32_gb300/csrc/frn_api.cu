@@ -70,7 +70,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-// Device status word of the stream kernel's bounded waits (one per device).
+// Device status word of the kernels' bounded waits (one per device).
 __device__ unsigned int g_frn_status_word;
 
 namespace {
@@ -360,10 +360,8 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
     unsigned int* status = nullptr;
-    if (kind == kStream) {
-        frn_status st = status_word(&status);
-        if (st != FRN_OK) return st;
-    }
+    frn_status st = status_word(&status);
+    if (st != FRN_OK) return st;
     const frn::Params p = make_params(c, rplan, splan, status);
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -154,16 +154,21 @@ __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Read a float from the shared memory of CTA `rank` of this cluster, at the
-// address that `local` has in this CTA's shared window.
-__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
-    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+// Shared-memory address of `local` in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
     uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote) : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+    return remote;
 }
+
+// Store a float into another CTA's shared memory and count its 4 bytes against
+// that CTA's mbarrier (the remote CTA waits on the barrier for the data).
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 ::"r"(remote_addr), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
+}
+
 
 // ------------------------------------------------------- number formats ----
 
@@ -285,6 +290,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
     return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity, giving up after about
+// limit_ns nanoseconds (returns false then).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
 }
 
 // 1-D bulk copy global -> shared (TMA, non-tensor form), completing `bytes`

@@ -1,14 +1,21 @@
-// frn_rows.cuh -- the row kernel: one token row per thread-block cluster.
+// frn_rows.cuh -- the row kernel: one token row per CTA or per thread-block
+// cluster.
 //
-// The tiles of a row are spread over C CTAs of one cluster (tiles_per_cta
-// warps each, one tile per warp).  For decode-sized T this puts one row on up
-// to 8 SMs, so a handful of tokens still engages most of the GPU.  Every thread
-// issues all of its R+1 128-bit loads (partials through the read-only path, no
-// L1 allocation, 256-byte L2 prefetch) before its first add, so each byte of
-// HBM is read exactly once and the row stays in registers until y is written.
-// Tile sums cross CTAs through distributed shared memory after one cluster
-// barrier; a second (split) barrier keeps each CTA's shared memory alive until
-// its peers have read it.
+// The tiles of a row go to one CTA (up to 1024 threads) or are spread over C
+// CTAs of one cluster (tiles_per_cta warps each, one tile per warp).  For
+// decode-sized T the cluster puts one row on up to 8 SMs, so a handful of
+// tokens still engages most of the GPU.  Every thread issues all of its R+1
+// 128-bit loads (partials through the read-only path, no L1 allocation,
+// 256-byte L2 prefetch) before its first add, so each byte of HBM is read
+// exactly once and the row stays in registers until y is written.
+//
+// In a cluster, each warp pushes its tile sum straight into every CTA's shared
+// memory with st.async, counted on that CTA's row mbarrier, and each CTA waits
+// (bounded) on its own barrier: one one-way hop instead of a cluster barrier
+// followed by remote reads.  The barriers are armed at kernel start, and the
+// cluster barrier that publishes them is waited on only after the loads, so
+// its latency hides behind DRAM.  A last split barrier keeps every CTA of the
+// cluster resident until all of them are done.
 #pragma once
 
 #include "frn_common.cuh"
@@ -21,7 +28,9 @@ namespace frn {
 // to 32 tiles (H <= 8192, R <= 8: 64 registers a thread).
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
 __global__ void __launch_bounds__(MAXT) frn_row_kernel(const __grid_constant__ Params p) {
-    __shared__ float tile_sum[MAXT / 32];
+    // single CTA: this CTA's tile sums; cluster: every tile sum of the row
+    __shared__ float tile_sum[CLUSTER ? kMaxTiles : MAXT / 32];
+    __shared__ __align__(8) uint64_t row_bar;   // cluster: counts the pushed tile sums
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -37,6 +46,19 @@ __global__ void __launch_bounds__(MAXT) frn_row_kernel(const __grid_constant__ P
     const int j = tile * kTileVecs + lane;              // vector index in the row
     const bool valid = j < p.nvec;
     const long long off = row * static_cast<long long>(p.nvec) + j;
+
+    if constexpr (CLUSTER) {
+        // Arm this CTA's row barrier for the 4-byte sums of all ntiles tiles
+        // before any CTA may push one: pushes start only after the cluster
+        // barrier this arrival belongs to.  No global memory is touched yet.
+        if (threadIdx.x == 0) {
+            mbar_init(smem_addr(&row_bar), 1);
+            mbar_init_fence();
+            mbar_arrive_expect_tx(smem_addr(&row_bar), 4u * static_cast<uint32_t>(p.ntiles));
+        }
+        __syncwarp();
+        cluster_arrive_release();
+    }
 
     // Nothing of the previous kernel on the stream may be read (or overwritten)
     // before it has completed.
@@ -59,29 +81,29 @@ __global__ void __launch_bounds__(MAXT) frn_row_kernel(const __grid_constant__ P
     const uint4 ro = pack8(acc);
 
     const float s = tile_sumsq(ro);
-    if (lane == 0) tile_sum[warp] = s;
-    __syncwarp();
 
-    // Every global store of this thread comes after the cluster arrivals below:
-    // a release arrival waits for all of the thread's earlier memory operations,
-    // and it only has to cover the tile sums and the DSMEM reads.
+    // Every global store of this thread comes after the cluster synchronisation
+    // below, so that no barrier operation waits for outstanding stores.
     float lo, hi;   // tile slots `lane` and `lane + 32` of the row
     if constexpr (CLUSTER) {
-        cluster_arrive_release();
-        cluster_wait_acquire();
-        const int tpc = p.tiles_per_cta;
-        lo = lane < p.ntiles ? ld_dsmem(&tile_sum[lane % tpc], lane / tpc) : 0.0f;
-        hi = lane + 32 < p.ntiles ? ld_dsmem(&tile_sum[(lane + 32) % tpc], (lane + 32) / tpc) : 0.0f;
+        cluster_wait_acquire();   // every CTA of the cluster has armed its row barrier
+        if (tile < p.ntiles && lane < p.ctas_per_row)
+            st_async_f32(cluster_addr(&tile_sum[tile], static_cast<uint32_t>(lane)), s,
+                         cluster_addr(&row_bar, static_cast<uint32_t>(lane)));
+        if (!mbar_wait_bounded(smem_addr(&row_bar), 0u, p.wait_limit_ns) && lane == 0 && p.error_word)
+            atomicOr(p.error_word, kErrWaitTimeout);
+        lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
+        hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     } else {
+        if (lane == 0) tile_sum[warp] = s;
         __syncthreads();
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
         hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     }
-    // rstd consumes lo and hi, so the DSMEM reads have completed before the
-    // relaxed arrival below tells the other CTAs they may exit (matching wait
-    // at the end); no release, hence no wait on anything else.
     const float rstd = row_rstd(lo, hi, p.H, p.eps);
     if constexpr (CLUSTER) {
+        // all sums pushed into this CTA have landed; the matching wait at the
+        // end keeps the cluster resident until every CTA got this far
         __syncwarp();
         cluster_arrive_relaxed_after(rstd);
     }
