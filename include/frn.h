@@ -260,8 +260,9 @@ int frn_version(void);
  * frn_set_ctas_per_row: row kernel only.  0 (default) chooses from T, H, R
  *   and the SM count between one CTA per row and a cluster of CTAs per row;
  *   1 forces one CTA per row (up to 1024 threads when H <= 8192 and R <= 8,
- *   else the smallest cluster that holds the row); 2..8 force a cluster of
- *   that many CTAs (rounded so that no CTA is empty).
+ *   else the smallest cluster that holds the row); 2..16 force a cluster of
+ *   that many CTAs (rounded so that no CTA is empty; 9..16 is a non-portable
+ *   cluster size, with at least two tiles a CTA).
  * frn_set_stream_groups: stream kernel only.  0 (default) chooses how many
  *   consumer groups (each taking every n-th row of a CTA, so that one group's
  *   epilogue overlaps the next group's loads) from H; 1..4 forces it, reduced

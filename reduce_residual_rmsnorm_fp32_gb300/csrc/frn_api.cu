@@ -10,6 +10,7 @@
 // layernorm.py).  Tuples become named output pointers, and the pages' "return
 // None to fall back" becomes an error status: there is no fallback path.
 #include <atomic>
+#include <cstdlib>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -109,25 +110,36 @@ frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     const int nvec = H / frn::kVecElems;
     const int ntiles = ceil_div(nvec, frn::kTileVecs);
     const int cmin = ceil_div(ntiles, frn::kMaxTilesPerCta);
-    const int cmax = ntiles < 8 ? ntiles : 8;
     int C;
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
     if (forced == 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
-    // From 40 rows on, a row wider than one 512-thread CTA goes to a single wide
-    // CTA: with that many rows the GPU is busy anyway, and the cluster launch
-    // and its barriers cost more than the extra SMs per row gain.
-    if (forced == 0 && cmin > 1 && T >= 40 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
     if (forced > 0) {
+        // up to 8 CTAs per cluster with at least one tile each; up to 16
+        // (non-portable cluster size) with at least two tiles each
+        const int cmax = ntiles < 8 ? ntiles : (forced > 8 ? (ntiles / 2 < 16 ? ntiles / 2 : 16) : 8);
         C = forced < cmin ? cmin : (forced > cmax ? cmax : forced);
-    } else if (cmin == 1) {
-        // The row fits one CTA: no cluster (a cluster launch and its barriers
-        // cost more than spreading a small row gains).
-        C = 1;
-    } else {
-        // The row needs a cluster anyway: spread it over more SMs (down to 4
-        // warps per CTA) while the rows still leave SMs idle.
+    } else if (T >= 128) {
+        // Many rows: one CTA per row (a wide one when the row needs more than
+        // 512 threads), or the smallest cluster that holds the row.
+        if (cmin > 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
         C = cmin;
-        while (C < cmax && T * (C + 1) <= num_sms && ceil_div(ntiles, C + 1) >= 4) ++C;
+    } else {
+        // Few rows: spread each row over a cluster of about 3 * #SMs / T CTAs
+        // of at least 4 warps (measured best at H = 4096 and 7168 for T < 128:
+        // tile sums travel by st.async, so a cluster costs little).
+        const int cmax = ntiles / 4 < 8 ? (ntiles / 4 > 1 ? ntiles / 4 : 1) : 8;
+        long long want = 3LL * num_sms / (T > 0 ? T : 1);
+        C = static_cast<int>(want < cmin ? cmin : (want > cmax ? cmax : want));
+        if (C < cmin) C = cmin;
+        // prefer a cluster size that splits the tiles evenly (the nearest
+        // divisor of ntiles in range, the larger on a tie): a ragged last CTA
+        // measured up to 25% slower at H = 16384
+        int best = 0;
+        for (int c = cmin; c <= (cmax > cmin ? cmax : cmin); ++c) {
+            if (ntiles % c) continue;
+            if (!best || std::abs(c - C) <= std::abs(best - C)) best = c;
+        }
+        if (best) C = best;
     }
     const int tpc = ceil_div(ntiles, C);
     C = ceil_div(ntiles, tpc);   // no empty CTA
@@ -588,8 +600,8 @@ FRN_EXPORT frn_status frn_set_pdl(int enable) {
 }
 
 FRN_EXPORT frn_status frn_set_ctas_per_row(int ctas_per_row) {
-    if (ctas_per_row < 0 || ctas_per_row > 8)
-        return fail(FRN_ERR_INVALID_ARG, "ctas_per_row=%d must be 0..8", ctas_per_row);
+    if (ctas_per_row < 0 || ctas_per_row > 16)
+        return fail(FRN_ERR_INVALID_ARG, "ctas_per_row=%d must be 0..16", ctas_per_row);
     g_force_ctas.store(ctas_per_row, std::memory_order_relaxed);
     return ok();
 }

@@ -18,6 +18,8 @@
 // cluster resident until all of them are done.
 #pragma once
 
+#include <atomic>
+
 #include "frn_common.cuh"
 
 namespace frn {
@@ -145,6 +147,21 @@ struct RowPlan {
 
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
 cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
+    if constexpr (CLUSTER) {
+        if (plan.ctas_per_row > 8) {
+            // clusters of 9..16 CTAs are a non-portable size: opt in once per device
+            static std::atomic<int> opted[64];
+            int dev = 0;
+            cudaError_t e = cudaGetDevice(&dev);
+            if (e != cudaSuccess) return e;
+            if (dev < 0 || dev >= 64 || !opted[dev].load(std::memory_order_acquire)) {
+                e = cudaFuncSetAttribute(frn_row_kernel<RMAX, MODE, CLUSTER, MAXT>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+                if (dev >= 0 && dev < 64) opted[dev].store(1, std::memory_order_release);
+            }
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);

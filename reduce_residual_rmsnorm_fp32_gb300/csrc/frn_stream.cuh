@@ -31,6 +31,8 @@
 // the CTA exits.
 #pragma once
 
+#include <atomic>
+
 #include "frn_common.cuh"
 
 namespace frn {
@@ -258,15 +260,15 @@ struct StreamPlan {
 
 template <int TPW, int MODE, int MAXTHREADS>
 cudaError_t launch_stream_one(const Params& p, const StreamPlan& plan, cudaStream_t stream, bool pdl) {
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(frn_stream_kernel<TPW, MODE, MAXTHREADS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmemLimit);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = 1;
+        if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);

@@ -105,7 +105,7 @@ def test_empty_T_is_ok_without_device(lib):
 
 def test_launch_controls(lib):
     assert lib.frn_set_pdl(0) == frn.FRN_OK and lib.frn_set_pdl(1) == frn.FRN_OK
-    assert lib.frn_set_ctas_per_row(9) == frn.FRN_ERR_INVALID_ARG
+    assert lib.frn_set_ctas_per_row(17) == frn.FRN_ERR_INVALID_ARG
     assert lib.frn_set_ctas_per_row(3) == frn.FRN_OK and lib.frn_set_ctas_per_row(0) == frn.FRN_OK
 
 

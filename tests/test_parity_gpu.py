@@ -164,7 +164,7 @@ def test_prefill_each_kernel(kernel):
     check_quant(inp, f"prefill kernel={kernel}", rows=sample_rows(inp.T, 32, seed=kernel))
 
 
-@pytest.mark.parametrize("ctas", [1, 2, 3, 4, 5, 7, 8, "stream"])
+@pytest.mark.parametrize("ctas", [1, 2, 3, 4, 5, 7, 8, 14, 16, "stream"])
 @pytest.mark.parametrize("H", [7168, 4096, 16384])
 def test_every_launch_shape_is_bit_identical(ctas, H):
     """Whatever number of CTAs a row is split over, and whichever kernel runs, every
