@@ -252,7 +252,8 @@ int frn_version(void);
  * frn_set_pdl: 1 (default) launches with programmatic dependent launch, so
  *   the kernel's prologue may overlap the tail of the previous kernel on the
  *   stream; the kernel still waits for that kernel's completion before its
- *   first global-memory access.  0 launches plainly.
+ *   first global-memory load or store (only an L2 prefetch hint, which hands
+ *   no value to the kernel, may precede the wait).  0 launches plainly.
  * frn_set_kernel: 0 (default) picks the kernel from T, H and the SM count;
  *   1 forces the row kernel (one row per thread-block cluster, for few rows),
  *   2 forces the stream kernel (persistent, one CTA per SM, rows streamed
@@ -267,8 +268,13 @@ int frn_version(void);
  *   consumer groups (each taking every n-th row of a CTA, so that one group's
  *   epilogue overlaps the next group's loads) from H; 1..4 forces it, reduced
  *   where the CTA would exceed 16 warps.
+ * frn_set_l2_prefetch: row kernel only.  0 (default) decides from the launch
+ *   shape whether each warp asks for its slice of the row to be fetched into
+ *   L2 before the wait on the previous kernel (a hint that hands no value to
+ *   the kernel); 1 never does, 2 always does.
  */
 frn_status frn_set_pdl(int enable);
+frn_status frn_set_l2_prefetch(int mode);
 frn_status frn_set_kernel(int kernel);
 frn_status frn_set_ctas_per_row(int ctas_per_row);
 frn_status frn_set_stream_groups(int groups);

@@ -72,6 +72,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_version.restype = i32
     lib.frn_set_pdl.argtypes = [i32]
     lib.frn_set_pdl.restype = i32
+    lib.frn_set_l2_prefetch.argtypes = [i32]
+    lib.frn_set_l2_prefetch.restype = i32
     lib.frn_set_ctas_per_row.argtypes = [i32]
     lib.frn_set_ctas_per_row.restype = i32
     lib.frn_set_kernel.argtypes = [i32]
@@ -131,6 +133,11 @@ def _check(status: int) -> None:
 
 def set_pdl(enable: bool) -> None:
     _check(library().frn_set_pdl(1 if enable else 0))
+
+
+def set_l2_prefetch(mode: int) -> None:
+    """Row kernel: 0 decide from the launch shape, 1 never, 2 always prefetch the row into L2."""
+    _check(library().frn_set_l2_prefetch(int(mode)))
 
 
 def set_ctas_per_row(n: int) -> None:

@@ -25,6 +25,7 @@ namespace {
 
 thread_local char g_detail[256] = "";
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_prefetch{0};   // 0 auto, 1 never, 2 always
 std::atomic<int> g_force_ctas{0};
 std::atomic<int> g_force_kernel{0};
 std::atomic<int> g_force_groups{0};
@@ -118,28 +119,35 @@ frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
         // (non-portable cluster size) with at least two tiles each
         const int cmax = ntiles < 8 ? ntiles : (forced > 8 ? (ntiles / 2 < 16 ? ntiles / 2 : 16) : 8);
         C = forced < cmin ? cmin : (forced > cmax ? cmax : forced);
-    } else if (T >= 128) {
-        // Many rows: one CTA per row (a wide one when the row needs more than
-        // 512 threads), or the smallest cluster that holds the row.
-        if (cmin > 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
-        C = cmin;
     } else {
-        // Few rows: spread each row over a cluster of about 3 * #SMs / T CTAs
-        // of at least 4 warps (measured best at H = 4096 and 7168 for T < 128:
-        // tile sums travel by st.async, so a cluster costs little).
-        const int cmax = ntiles / 4 < 8 ? (ntiles / 4 > 1 ? ntiles / 4 : 1) : 8;
-        long long want = 3LL * num_sms / (T > 0 ? T : 1);
-        C = static_cast<int>(want < cmin ? cmin : (want > cmax ? cmax : want));
-        if (C < cmin) C = cmin;
-        // prefer a cluster size that splits the tiles evenly (the nearest
-        // divisor of ntiles in range, the larger on a tie): a ragged last CTA
-        // measured up to 25% slower at H = 16384
-        int best = 0;
-        for (int c = cmin; c <= (cmax > cmin ? cmax : cmin); ++c) {
-            if (ntiles % c) continue;
-            if (!best || std::abs(c - C) <= std::abs(best - C)) best = c;
+        // One CTA per row (a wide one when the row needs more than 512
+        // threads), or the smallest cluster that holds the row -- except for a
+        // few rows of more than 96 KB of loads each, which go to a cluster of
+        // up to 4 CTAs so that about 64 CTAs share the work (measured with the
+        // L2 prefetch at H = 4096..16384, R = 2..8, T = 8..128: larger
+        // clusters and more CTAs cost more in synchronisation than they gain).
+        const long long row_bytes = 2LL * H * (R + 1);
+        int want = 1;
+        if (row_bytes > 96 * 1024 && T < 64) {
+            want = static_cast<int>(64 / T);
+            if (want > 4) want = 4;
         }
-        if (best) C = best;
+        if (want <= 1) {
+            if (cmin > 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
+            C = cmin;
+        } else {
+            // prefer a size that splits the tiles evenly (the nearest divisor of
+            // ntiles, the larger on a tie): a ragged last CTA measured up to 25%
+            // slower at H = 16384
+            if (want < cmin) want = cmin;
+            C = want;
+            int best = 0;
+            for (int c = cmin; c <= want; ++c) {
+                if (ntiles % c) continue;
+                if (!best || std::abs(c - want) <= std::abs(best - want)) best = c;
+            }
+            if (best) C = best;
+        }
     }
     const int tpc = ceil_div(ntiles, C);
     C = ceil_div(ntiles, tpc);   // no empty CTA
@@ -365,6 +373,17 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 
 // The fused epilogue (one kernel).  quant as in Call; the kernel writes c.y
 // when it is not NULL.
+// The L2 prefetch pays when the grid is at most about two waves (most CTAs
+// start while the previous kernel on the stream drains, or while the first
+// wave runs), and each CTA loads at least 48 KB or the grid has at least 64
+// CTAs (measured: below both, the extra requests cost more than the overlap
+// gives; beyond two waves it gains nothing).
+bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms) {
+    if (plan.grid * plan.threads > 2048LL * sms) return false;
+    const long long cta_bytes = 2LL * H * (R + 1) / plan.ctas_per_row;
+    return cta_bytes >= 48 * 1024 || T * plan.ctas_per_row >= 64;
+}
+
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
     const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
@@ -374,7 +393,11 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     unsigned int* status = nullptr;
     frn_status st = status_word(&status);
     if (st != FRN_OK) return st;
-    const frn::Params p = make_params(c, rplan, splan, status);
+    frn::Params p = make_params(c, rplan, splan, status);
+    // decode-sized grids (every CTA resident at once, so each starts while the
+    // previous kernel drains): prefetch the row into L2 before the dependency wait
+    const int pf = g_prefetch.load(std::memory_order_relaxed);
+    p.prefetch_l2 = kind == kRows && (pf == 2 || (pf == 0 && prefetch_pays(rplan, c.T, c.H, c.R, sms)));
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -593,6 +616,12 @@ FRN_EXPORT const char* frn_status_string(frn_status s) {
 FRN_EXPORT const char* frn_last_error_detail(void) { return g_detail; }
 
 FRN_EXPORT int frn_version(void) { return 100; }
+
+FRN_EXPORT frn_status frn_set_l2_prefetch(int mode) {
+    if (mode < 0 || mode > 2) return fail(FRN_ERR_INVALID_ARG, "l2 prefetch mode=%d must be 0..2", mode);
+    g_prefetch.store(mode, std::memory_order_relaxed);
+    return ok();
+}
 
 FRN_EXPORT frn_status frn_set_pdl(int enable) {
     g_pdl.store(enable ? 1 : 0, std::memory_order_relaxed);

@@ -64,6 +64,7 @@ struct Params {
     int H;
     int nvec;                // H / 8
     int ntiles;              // ceil(nvec / 32)
+    int prefetch_l2;         // row kernel: prefetch the row into L2 before the grid dependency wait
     int tiles_per_cta;       // warps per CTA
     int ctas_per_row;        // cluster size (row kernel)
     float eps;
@@ -309,6 +310,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Ask the TMA unit to bring [src, src + bytes) into L2 (16-byte aligned, a
+// multiple of 16 bytes).  A hint only: no register receives data from it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------- per-vector arithmetic ----

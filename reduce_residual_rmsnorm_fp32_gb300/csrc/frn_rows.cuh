@@ -2,9 +2,9 @@
 // cluster.
 //
 // The tiles of a row go to one CTA (up to 1024 threads) or are spread over C
-// CTAs of one cluster (tiles_per_cta warps each, one tile per warp).  For
-// decode-sized T the cluster puts one row on up to 8 SMs, so a handful of
-// tokens still engages most of the GPU.  Every thread issues all of its R+1
+// CTAs of one cluster (tiles_per_cta warps each, one tile per warp): a row too
+// wide for one CTA, or one of a few heavy decode rows, so that a handful of
+// tokens still spreads over several SMs.  Every thread issues all of its R+1
 // 128-bit loads (partials through the read-only path, no L1 allocation,
 // 256-byte L2 prefetch) before its first add, so each byte of HBM is read
 // exactly once and the row stays in registers until y is written.
@@ -60,6 +60,22 @@ __global__ void __launch_bounds__(MAXT) frn_row_kernel(const __grid_constant__ P
         }
         __syncwarp();
         cluster_arrive_release();
+    }
+
+    // When the whole grid is resident at once (decode-sized T), start the DRAM
+    // fetch of this warp's tile while the previous kernel on the stream is still
+    // finishing: lanes 0..R-1 prefetch the partials' spans, lane R the
+    // residual's, lane R+1 gamma's, into L2 only.  A prefetch hands no value to
+    // this kernel, and L2 is where the previous kernel's writes land, so every
+    // value read after the wait below is still the completed one.
+    if (p.prefetch_l2 && tile < p.ntiles && lane <= p.R + 1) {
+        const int first = tile * kTileVecs;
+        const int nv = p.nvec - first < kTileVecs ? p.nvec - first : kTileVecs;
+        const long long base = row * static_cast<long long>(p.nvec) + first;
+        const uint4* src = lane < p.R ? p.partials[lane] + base
+                         : lane == p.R ? (p.residual != nullptr ? p.residual + base : nullptr)
+                                       : p.gamma + first;
+        if (src != nullptr) bulk_prefetch_l2(src, 16u * static_cast<uint32_t>(nv));
     }
 
     // Nothing of the previous kernel on the stream may be read (or overwritten)

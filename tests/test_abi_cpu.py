@@ -107,6 +107,8 @@ def test_launch_controls(lib):
     assert lib.frn_set_pdl(0) == frn.FRN_OK and lib.frn_set_pdl(1) == frn.FRN_OK
     assert lib.frn_set_ctas_per_row(17) == frn.FRN_ERR_INVALID_ARG
     assert lib.frn_set_ctas_per_row(3) == frn.FRN_OK and lib.frn_set_ctas_per_row(0) == frn.FRN_OK
+    assert lib.frn_set_l2_prefetch(3) == frn.FRN_ERR_INVALID_ARG and lib.frn_set_l2_prefetch(-1) == frn.FRN_ERR_INVALID_ARG
+    assert lib.frn_set_l2_prefetch(1) == frn.FRN_OK and lib.frn_set_l2_prefetch(0) == frn.FRN_OK
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device error path; a GPU would run the call")

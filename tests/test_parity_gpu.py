@@ -186,6 +186,28 @@ def test_every_launch_shape_is_bit_identical(ctas, H):
         assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
 
+@pytest.mark.parametrize("prefetch", [1, 2])
+@pytest.mark.parametrize("ctas", [1, 3, 8])
+@pytest.mark.parametrize("H", [7000, 16384, 2056])
+def test_l2_prefetch_changes_no_bit(prefetch, ctas, H):
+    """The L2 prefetch before the dependency wait (off, or forced on for every
+    row launch, over ragged last tiles too) leaves every output bit as it is."""
+    inp = syn.make_inputs(8, 13, H, seed=6, partial_std=0.5)
+    d = DevInputs(inp)
+    frn.set_kernel(frn.KERNEL_ROWS)
+    frn.set_ctas_per_row(ctas)
+    try:
+        base = gpu_quant(d, True) if H % 128 == 0 else gpu_norm(d)
+        frn.set_l2_prefetch(prefetch)
+        got = gpu_quant(d, True) if H % 128 == 0 else gpu_norm(d)
+    finally:
+        frn.set_l2_prefetch(0)
+        frn.set_ctas_per_row(0)
+        frn.set_kernel(frn.KERNEL_AUTO)
+    for a, b in zip(base, got):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
 # ------------------------------------------------------------- edge cases --
 
 def test_empty_T_is_noop():
