@@ -27,9 +27,17 @@ namespace frn {
 // RMAX is the unrolled partial count (R <= RMAX; loads beyond R are predicated
 // off).  CLUSTER == false is the single-CTA row (no cluster barriers).  MAXT is
 // the launch bound: 512 threads (16 tiles), or 1024 for a single-CTA row of up
-// to 32 tiles (H <= 8192, R <= 8: 64 registers a thread).
+// to 32 tiles (H <= 8192, R <= 8: 64 registers a thread).  The second bound
+// holds the register count where the row count per SM needs it: R <= 2 at
+// 32 registers (two wide or four 512-thread rows per SM: the prefill shapes
+// live on that), R <= 4 at 40 (three 512-thread rows), R <= 8 at 64.
+constexpr int row_min_blocks(int rmax, int maxt) {
+    return maxt > kMaxThreads ? (rmax <= 2 ? 2 : 1) : (rmax <= 2 ? 4 : rmax <= 4 ? 3 : rmax <= 8 ? 2 : 1);
+}
+
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
-__global__ void __launch_bounds__(MAXT) frn_row_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(MAXT, row_min_blocks(RMAX, MAXT))
+frn_row_kernel(const __grid_constant__ Params p) {
     // single CTA: this CTA's tile sums; cluster: every tile sum of the row
     __shared__ float tile_sum[CLUSTER ? kMaxTiles : MAXT / 32];
     __shared__ __align__(8) uint64_t row_bar;   // cluster: counts the pushed tile sums
