@@ -30,7 +30,8 @@
  *                  (fp32 adds, rank order 0..R-1, residual last)
  *   residual_out = bf16_rn(x_hat)
  *   x            = f32(residual_out)
- *   y            = bf16_rn((x * rstd) * f32(gamma)),  rstd = 1/sqrt(sum(x^2)/H + eps)
+ *   y            = bf16_rn((x * f32(gamma)) * rstd),  rstd = 1/sqrt(sum(x^2)/H + eps)
+ *                  (x * gamma is exact in fp32; one fp32 rounding, then one to bf16)
  *   per group g of group_size consecutive elements of y:
  *     a = max |f32(y)|,  s = a / 448 (fp32),  q = e4m3fn_rn_satfinite(f32(y) / s),
  *     and q = 0 when s == 0.
@@ -270,8 +271,10 @@ int frn_version(void);
  *   where the CTA would exceed 16 warps.
  * frn_set_l2_prefetch: row kernel only.  0 (default) decides from the launch
  *   shape whether each warp asks for its slice of the row to be fetched into
- *   L2 before the wait on the previous kernel (a hint that hands no value to
- *   the kernel); 1 never does, 2 always does.
+ *   L2 before the wait on the previous kernel, and, for grids of more than
+ *   one wave, for the same slice of the row one wave ahead (hints that hand
+ *   no value to the kernel); 1 does neither; 2 always does the first and
+ *   decides the second as 0 does.
  */
 frn_status frn_set_pdl(int enable);
 frn_status frn_set_l2_prefetch(int mode);

@@ -398,6 +398,18 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // previous kernel drains): prefetch the row into L2 before the dependency wait
     const int pf = g_prefetch.load(std::memory_order_relaxed);
     p.prefetch_l2 = kind == kRows && (pf == 2 || (pf == 0 && prefetch_pays(rplan, c.T, c.H, c.R, sms)));
+    // More rows than one wave holds, with R <= 2 (few loads in flight per SM):
+    // each CTA prefetches the row about one wave ahead (the CTAs resident at
+    // 2048 threads an SM).  Measured on GB300 at H = 7168: +6% at T = 8192
+    // without quant, +4..5% at T = 512..1024; -1% for a y-less quant at
+    // T = 8192 (issue-bound there), so it is left out for those beyond four
+    // waves; with R >= 4 it cost 8..17% (enough loads in flight already).
+    if (kind == kRows && pf != 1 && c.R <= 2) {
+        const long long wave_rows = static_cast<long long>(2048 / rplan.threads) * sms / rplan.ctas_per_row;
+        const bool yless_quant = quant == 1 || quant == 3;
+        if (wave_rows > 0 && c.T > wave_rows && (!yless_quant || c.T <= 4 * wave_rows))
+            p.prefetch_ahead = wave_rows;
+    }
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;

@@ -5,7 +5,7 @@
 //
 // The op, per token row (include/frn.h has the full contract):
 //   x_hat = sum_r f32(P[r]) (rank order) + f32(residual);  residual_out = bf16(x_hat)
-//   y = bf16((x * rstd) * gamma),  rstd = 1/sqrt(sum(x^2)/H + eps),  x = f32(residual_out)
+//   y = bf16((x * gamma) * rstd),  rstd = 1/sqrt(sum(x^2)/H + eps),  x = f32(residual_out)
 //   per 128-group of y: s = max|y| / 448, q = e4m3(y / s)
 // following the replaced subgraph all_reduce -> (fused_add_)rms_norm of the
 // "ROCm AITER fused all-reduce + RMSNorm" page (vLLM PR 37646 summary, key source
@@ -65,6 +65,7 @@ struct Params {
     int nvec;                // H / 8
     int ntiles;              // ceil(nvec / 32)
     int prefetch_l2;         // row kernel: prefetch the row into L2 before the grid dependency wait
+    long long prefetch_ahead;  // row kernel: also prefetch the row this many rows ahead (0: no)
     int tiles_per_cta;       // warps per CTA
     int ctas_per_row;        // cluster size (row kernel)
     float eps;
@@ -337,13 +338,42 @@ __device__ __forceinline__ float row_rstd(float lo, float hi, int H, float eps) 
     return __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(H)), eps));
 }
 
-// y = bf16((x * rstd) * gamma) for one vector of bf16 x.
+// x * gamma for a packed bf16 pair of each, straight from the register halves:
+// the mixed-precision FMA with a -0 addend (-0 keeps the sign of a zero
+// product) rounds the exact product once, like an fp32 multiply of the widened
+// values; inside fp32's range the product of two bf16 values is exact.
+__device__ __forceinline__ void mul2_bf16(float& p0, float& p1, uint32_t xw, uint32_t gw) {
+    asm("{\n\t.reg .b16 xl, xh, gl, gh;\n\t"
+        "mov.b32 {xl, xh}, %2;\n\t"
+        "mov.b32 {gl, gh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, xl, gl, 0f80000000;\n\t"
+        "fma.rn.f32.bf16 %1, xh, gh, 0f80000000;\n\t}"
+        : "=f"(p0), "=f"(p1) : "r"(xw), "r"(gw));
+}
+
+// y = bf16(fl32((x * gamma) * rstd)) for one vector of bf16 x: x * gamma is
+// exact (inside fp32's range), so y takes one fp32 rounding of x * gamma * rstd
+// before the bf16 one.
+// MIXED forms x * gamma with the mixed-precision FMA (fewer instructions);
+// otherwise both are widened first and multiplied in fp32 (fewer live
+// registers in register-capped kernels).  The two give the same bits.
+template <bool MIXED = true>
 __device__ __forceinline__ uint4 rms_y(const uint4 xb, float rstd, const uint4 g) {
-    float x[8], gf[8], yv[8];
-    unpack8(xb, x);
-    unpack8(g, gf);
+    float yv[8];
+    if constexpr (MIXED) {
+        mul2_bf16(yv[0], yv[1], xb.x, g.x);
+        mul2_bf16(yv[2], yv[3], xb.y, g.y);
+        mul2_bf16(yv[4], yv[5], xb.z, g.z);
+        mul2_bf16(yv[6], yv[7], xb.w, g.w);
+    } else {
+        float gf[8];
+        unpack8(xb, yv);
+        unpack8(g, gf);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(__fmul_rn(x[i], rstd), gf[i]);
+        for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(yv[i], gf[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(yv[i], rstd);
     return pack8(yv);
 }
 
@@ -433,11 +463,18 @@ __device__ __forceinline__ void mxfp4_8(const uint4 yb, uint32_t& packed, uint32
         int shared = lg - 2;
         shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
         code = static_cast<uint32_t>(shared + 127);
-        const float inv = __int_as_float((127 - shared) << 23);   // 2^-shared; shared <= 125 for bf16 y
+        // 2^-shared as a bf16 pair: shared lies in [-127, 125] for bf16 y, so
+        // 2^-shared is a bf16 normal (exponent field 2..254).  y * 2^-shared is
+        // then one mixed-precision product per element, exact unless it falls
+        // among the fp32 subnormals, where it takes the same single rounding as
+        // an fp32 multiply.
+        const uint32_t inv16 = static_cast<uint32_t>(127 - shared) << 7;
+        const uint32_t inv2 = inv16 | (inv16 << 16);
         float v[8];
-        unpack8(yb, v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], inv);
+        mul2_bf16(v[0], v[1], yb.x, inv2);
+        mul2_bf16(v[2], v[3], yb.y, inv2);
+        mul2_bf16(v[4], v[5], yb.z, inv2);
+        mul2_bf16(v[6], v[7], yb.w, inv2);
         packed = pack_e2m1x2(v[0], v[1]) | (pack_e2m1x2(v[2], v[3]) << 8) | (pack_e2m1x2(v[4], v[5]) << 16) |
                  (pack_e2m1x2(v[6], v[7]) << 24);
     }

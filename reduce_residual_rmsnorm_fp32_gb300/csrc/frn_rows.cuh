@@ -24,19 +24,38 @@
 
 namespace frn {
 
+// Lanes 0..R-1 of a warp ask for the warp's tile of `row` of each partial to be
+// fetched into L2, lane R for the residual's, lane R+1 for gamma's (when
+// with_gamma).  Hints only: nothing reads a value from them.
+__device__ __forceinline__ void prefetch_tile_span(const Params& p, long long row, int tile, int lane,
+                                                   bool with_gamma) {
+    if (lane > p.R + (with_gamma ? 1 : 0)) return;
+    const int first = tile * kTileVecs;
+    const int nv = p.nvec - first < kTileVecs ? p.nvec - first : kTileVecs;
+    const long long base = row * static_cast<long long>(p.nvec) + first;
+    const uint4* src = lane < p.R ? p.partials[lane] + base
+                     : lane == p.R ? (p.residual != nullptr ? p.residual + base : nullptr)
+                                   : p.gamma + first;
+    if (src != nullptr) bulk_prefetch_l2(src, 16u * static_cast<uint32_t>(nv));
+}
+
 // RMAX is the unrolled partial count (R <= RMAX; loads beyond R are predicated
 // off).  CLUSTER == false is the single-CTA row (no cluster barriers).  MAXT is
 // the launch bound: 512 threads (16 tiles), or 1024 for a single-CTA row of up
 // to 32 tiles (H <= 8192, R <= 8: 64 registers a thread).  The second bound
-// holds the register count where the row count per SM needs it: R <= 2 at
-// 32 registers (two wide or four 512-thread rows per SM: the prefill shapes
-// live on that), R <= 4 at 40 (three 512-thread rows), R <= 8 at 64.
-constexpr int row_min_blocks(int rmax, int maxt) {
-    return maxt > kMaxThreads ? (rmax <= 2 ? 2 : 1) : (rmax <= 2 ? 4 : rmax <= 4 ? 3 : rmax <= 8 ? 2 : 1);
+// holds the register count of a single-CTA row where the row count per SM
+// needs it: R <= 2 at 32 registers (two wide or four 512-thread rows per SM:
+// the prefill shapes live on that), R <= 4 at 40 (three 512-thread rows),
+// R <= 8 at 64.  Cluster rows (H > 8192, or a few heavy decode rows) keep
+// what the compiler picks.
+constexpr int row_min_blocks(int rmax, bool cluster, int maxt) {
+    return cluster ? 1
+         : maxt > kMaxThreads ? (rmax <= 2 ? 2 : 1)
+                              : (rmax <= 2 ? 4 : rmax <= 4 ? 3 : rmax <= 8 ? 2 : 1);
 }
 
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
-__global__ void __launch_bounds__(MAXT, row_min_blocks(RMAX, MAXT))
+__global__ void __launch_bounds__(MAXT, row_min_blocks(RMAX, CLUSTER, MAXT))
 frn_row_kernel(const __grid_constant__ Params p) {
     // single CTA: this CTA's tile sums; cluster: every tile sum of the row
     __shared__ float tile_sum[CLUSTER ? kMaxTiles : MAXT / 32];
@@ -72,19 +91,14 @@ frn_row_kernel(const __grid_constant__ Params p) {
 
     // When the whole grid is resident at once (decode-sized T), start the DRAM
     // fetch of this warp's tile while the previous kernel on the stream is still
-    // finishing: lanes 0..R-1 prefetch the partials' spans, lane R the
-    // residual's, lane R+1 gamma's, into L2 only.  A prefetch hands no value to
-    // this kernel, and L2 is where the previous kernel's writes land, so every
-    // value read after the wait below is still the completed one.
-    if (p.prefetch_l2 && tile < p.ntiles && lane <= p.R + 1) {
-        const int first = tile * kTileVecs;
-        const int nv = p.nvec - first < kTileVecs ? p.nvec - first : kTileVecs;
-        const long long base = row * static_cast<long long>(p.nvec) + first;
-        const uint4* src = lane < p.R ? p.partials[lane] + base
-                         : lane == p.R ? (p.residual != nullptr ? p.residual + base : nullptr)
-                                       : p.gamma + first;
-        if (src != nullptr) bulk_prefetch_l2(src, 16u * static_cast<uint32_t>(nv));
-    }
+    // finishing.  A prefetch hands no value to this kernel, and L2 is where the
+    // previous kernel's writes land, so every value read after the wait below
+    // is still the completed one.
+    if (p.prefetch_l2 && tile < p.ntiles) prefetch_tile_span(p, row, tile, lane, true);
+    // Many rows: ask for the same tile of the row about one wave of CTAs ahead,
+    // so that the CTA which takes that row finds it in L2.
+    if (p.prefetch_ahead > 0 && tile < p.ntiles && row + p.prefetch_ahead < p.T)
+        prefetch_tile_span(p, row + p.prefetch_ahead, tile, lane, false);
 
     // Nothing of the previous kernel on the stream may be read (or overwritten)
     // before it has completed.

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
 #pragma unroll
         for (int t = 0; t < TPW; ++t) {
             const uint4 gt = kGammaInRegs ? g[kGammaInRegs ? t : 0] : ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
-            const uint4 yb = rms_y(rov[t], rstd, gt);
+            const uint4 yb = rms_y<false>(rov[t], rstd, gt);   // widened form: measured faster here
             if constexpr (mode_writes_y(MODE)) {
                 if (vt[t]) p.y[rbase + jt[t]] = yb;
             }
