@@ -192,19 +192,21 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
 //  * a row that fits one 512-thread CTA (H <= 4096): the row kernel at any T
 //    (several rows in flight per SM);
 //  * a row for a wide CTA (H <= 8192, R <= 8): the row kernel, except from
-//    2 rows per SM on where the stream kernel's overlap of one row's epilogue
-//    with the next rows' loads wins -- R >= 4, R == 1, or a variant that writes
-//    y and a quant (B) from 8 rows per SM on;
+//    2 rows per SM on with R != 2, where the stream kernel's overlap of one
+//    row's epilogue with the next rows' loads wins (with R = 2 the row kernel
+//    -- 32 registers, two rows per SM, one-wave-ahead L2 prefetch, rstd from
+//    one warp -- wins for every output variant; R = 3 unrolls as 4 and keeps
+//    one wide row per SM, 40% slower);
 //  * a wider row: the stream kernel from one row per SM on.
 int choose_kind(long long T, int H, int R, int quant, int num_sms) {
+    (void)quant;
     const int forced = g_force_kernel.load(std::memory_order_relaxed);
     if (forced == kRows || forced == kStream) return forced;
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
     if (ntiles <= frn::kMaxTilesPerCta) return kRows;
     if (wide_possible(ntiles, R)) {
         if (T < 2LL * num_sms) return kRows;
-        const bool heavy_b = (quant == 2 || quant == 4) && T >= 8LL * num_sms;
-        return (R >= 4 || R == 1 || heavy_b) ? kStream : kRows;
+        return R == 2 ? kRows : kStream;
     }
     return T >= num_sms ? kStream : kRows;
 }
@@ -398,6 +400,10 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // previous kernel drains): prefetch the row into L2 before the dependency wait
     const int pf = g_prefetch.load(std::memory_order_relaxed);
     p.prefetch_l2 = kind == kRows && (pf == 2 || (pf == 0 && prefetch_pays(rplan, c.T, c.H, c.R, sms)));
+    // Beyond about two waves the row kernel is issue-bound rather than
+    // latency-bound: warp 0 alone computes rstd (measured -1..4% time at
+    // T = 8192, H = 7168, R = 2; +2% at T = 32, where it is left off).
+    p.rstd_one_warp = kind == kRows && rplan.grid * rplan.threads > 2048LL * sms;
     // More rows than one wave holds, with R <= 2 (few loads in flight per SM):
     // each CTA prefetches the row about one wave ahead (the CTAs resident at
     // 2048 threads an SM).  Measured on GB300 at H = 7168: +6% at T = 8192

@@ -66,6 +66,7 @@ struct Params {
     int ntiles;              // ceil(nvec / 32)
     int prefetch_l2;         // row kernel: prefetch the row into L2 before the grid dependency wait
     long long prefetch_ahead;  // row kernel: also prefetch the row this many rows ahead (0: no)
+    int rstd_one_warp;       // single-CTA row kernel: warp 0 alone computes rstd and shares it
     int tiles_per_cta;       // warps per CTA
     int ctas_per_row;        // cluster size (row kernel)
     float eps;

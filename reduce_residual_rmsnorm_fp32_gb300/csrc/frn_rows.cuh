@@ -140,7 +140,22 @@ frn_row_kernel(const __grid_constant__ Params p) {
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
         hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     }
-    const float rstd = row_rstd(lo, hi, p.H, p.eps);
+    float rstd;
+    if (!CLUSTER && p.rstd_one_warp) {
+        // Many rows: warp 0 alone finishes the reduction and hands rstd to the
+        // others through shared memory -- one more barrier, but the butterfly,
+        // divide and square root leave every other warp's issue slots free for
+        // the CTAs that share the SM.  Same tree, same bits.
+        __shared__ float rstd_sh;
+        if (warp == 0) {
+            const float r0 = row_rstd(lo, hi, p.H, p.eps);
+            if (lane == 0) rstd_sh = r0;
+        }
+        __syncthreads();
+        rstd = rstd_sh;
+    } else {
+        rstd = row_rstd(lo, hi, p.H, p.eps);
+    }
     if constexpr (CLUSTER) {
         // all sums pushed into this CTA have landed; the matching wait at the
         // end keeps the cluster resident until every CTA got this far
