@@ -186,6 +186,28 @@ def test_every_launch_shape_is_bit_identical(ctas, H):
         assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
 
+@pytest.mark.parametrize("R", [2, 8])
+def test_many_row_launches_are_bit_identical(R):
+    """At 400 rows (beyond two waves of wide CTAs: rstd from one warp, and with
+    R = 2 the one-wave-ahead L2 prefetch) the row kernel gives the bits of the
+    stream kernel, and its first rows the bits of a 13-row call of the same
+    rows (per-warp rstd, no ahead prefetch)."""
+    inp = syn.make_inputs(R, 400, 7168, seed=8, partial_std=0.5)
+    d = DevInputs(inp)
+    few = DevInputs(syn.Inputs(inp.partials[:, :13], inp.residual[:13], inp.gamma, inp.eps))
+    try:
+        frn.set_kernel(frn.KERNEL_ROWS)
+        rows = gpu_quant(d, True)
+        rows_few = gpu_quant(few, True)
+        frn.set_kernel(frn.KERNEL_STREAM)
+        stream = gpu_quant(d, True)
+    finally:
+        frn.set_kernel(frn.KERNEL_AUTO)
+    for a, b, c in zip(rows, stream, rows_few):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+        assert np.array_equal(np.asarray(a)[:13].view(np.uint8), np.asarray(c).view(np.uint8))
+
+
 @pytest.mark.parametrize("prefetch", [1, 2])
 @pytest.mark.parametrize("ctas", [1, 3, 8])
 @pytest.mark.parametrize("H", [7000, 16384, 2056])
