@@ -455,9 +455,45 @@ def cpu_baseline(seconds: float = 12.0):
         el = time.perf_counter() - t0
         if el >= seconds or steps >= 1000:
             break
+    # the same oracle on one thread, for a few seconds
+    nb1, st1 = 0, 0
+    t1 = time.perf_counter()
+    while True:
+        for inp in inps:
+            orc.reduce_rmsnorm(inp.partials, inp.residual, inp.gamma, inp.eps, threads=1)
+        st1 += 1
+        nb1 += step_bytes()
+        el1 = time.perf_counter() - t1
+        if el1 >= seconds / 4 or st1 >= 1000:
+            break
     return {"value": round(nbytes / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{steps} whole decode steps (T=8,16,32,64; R=8, H=7168), OpenMP rows over {cores} threads, "
-                      f"{el:.1f} s"}
+                      f"{el:.1f} s",
+            "single_thread": {"value": round(nb1 / el1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{st1} whole decode steps on one thread, {el1:.1f} s"},
+            "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu prints it (or /proc/cpuinfo), and the core count."""
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not name:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    name = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return f"{name or 'unknown'} ({os.cpu_count()} cores)"
 
 
 # ------------------------------------------------------------ reference --
