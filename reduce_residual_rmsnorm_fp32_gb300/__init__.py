@@ -21,6 +21,7 @@ Entry points (same names as the C ABI):
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -176,14 +177,19 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else t.data_ptr()
 
 
-def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, device: torch.device) -> None:
+def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, device: torch.device,
+                  out: bool = False) -> None:
+    """Inputs must be on the call's CUDA device; an output (out=True) may also be
+    a pinned host tensor, which the kernel writes over the host link."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device != device or t.device.type != "cuda":
-        raise ValueError(f"{name} must be on {device} (got {t.device})")
+    if t.device != device or device.type != "cuda":
+        if not (out and device.type == "cuda" and t.device.type == "cpu" and t.is_pinned()):
+            raise ValueError(f"{name} must be on {device}" + (" or in pinned host memory" if out else "") +
+                             f" (got {t.device})")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -208,10 +214,23 @@ def _partials(partials) -> tuple[list[int], int, int, int, torch.device]:
     return [p.data_ptr() for p in parts], len(parts), T, H, dev
 
 
+# The current stream's raw handle without building a Stream object (a few
+# microseconds less per call); the public route where torch lacks it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_SAME_DEVICE = contextlib.nullcontext()
+
+
 def _stream(stream, device) -> int | None:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(device.index)
         stream = torch.cuda.current_stream(device)
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _on(device):
+    """The call's device as the current one (a no-op when it already is)."""
+    return _SAME_DEVICE if torch.cuda.current_device() == device.index else torch.cuda.device(device)
 
 
 def fused_reduce_rmsnorm(partials: torch.Tensor | Sequence[torch.Tensor], residual: torch.Tensor | None,
@@ -226,10 +245,10 @@ def fused_reduce_rmsnorm(partials: torch.Tensor | Sequence[torch.Tensor], residu
         residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     if y is None:
         y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
-    _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev, out=True)
+    _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
     arr = (ctypes.c_void_p * R)(*ptrs)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().fused_reduce_rmsnorm(arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y),
                                             T, H, float(eps), _stream(stream, dev))
     _check(st)
@@ -259,15 +278,15 @@ def fused_reduce_rmsnorm_quant_per_group(partials, residual: torch.Tensor | None
         q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=dev)
     if scales is None:
         scales = torch.empty((T, H // group_size), dtype=torch.float32, device=dev)
-    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev, out=True)
     if y is not None:
-        _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
+        _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
     if q.dtype not in (torch.float8_e4m3fn, torch.uint8):
         raise TypeError("q must be float8_e4m3fn or uint8")
-    _check_tensor(q, "q", q.dtype, (T, H), dev)
-    _check_tensor(scales, "scales", torch.float32, (T, H // group_size), dev)
+    _check_tensor(q, "q", q.dtype, (T, H), dev, out=True)
+    _check_tensor(scales, "scales", torch.float32, (T, H // group_size), dev, out=True)
     arr = (ctypes.c_void_p * R)(*ptrs)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().fused_reduce_rmsnorm_quant_per_group(
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales),
             T, H, float(eps), int(group_size), _stream(stream, dev))
@@ -313,7 +332,7 @@ def unfused_reduce_rmsnorm(partials, residual: torch.Tensor | None, gamma: torch
         if scales is None:
             scales = torch.empty((T, H // group_size), dtype=torch.float32, device=dev)
     arr = (ctypes.c_void_p * R)(*ptrs)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().frn_unfused_reduce_rmsnorm(
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q) if quant else None,
             _ptr(scales) if quant else None, T, H, float(eps), int(group_size), int(stages), _ptr(workspace),
@@ -338,7 +357,7 @@ def unfused_reduce_rmsnorm_noalloc(partials, residual: torch.Tensor | None, gamm
     scratch."""
     ptrs, R, T, H, dev = _partials(partials)
     arr = (ctypes.c_void_p * R)(*ptrs)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().frn_unfused_reduce_rmsnorm_noalloc(
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales), T, H,
             float(eps), int(group_size), int(stages), _stream(stream, dev))
@@ -356,9 +375,9 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None, gamma: tor
     _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
     residual_out = torch.empty_like(x) if residual_out is None else residual_out
     y = torch.empty_like(x) if y is None else y
-    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
-    _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
-    with torch.cuda.device(dev):
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev, out=True)
+    _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
+    with _on(dev):
         st = library().frn_fused_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), T,
                                              H, float(eps), _stream(stream, dev))
     _check(st)
@@ -373,8 +392,8 @@ def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, *, y: torch
     _check_tensor(x, "x", torch.bfloat16, (T, H), dev)
     _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
     y = torch.empty_like(x) if y is None else y
-    _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
-    with torch.cuda.device(dev):
+    _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
+    with _on(dev):
         st = library().frn_rmsnorm(_ptr(x), _ptr(gamma), _ptr(y), T, H, float(eps), _stream(stream, dev))
     _check(st)
     return y
@@ -401,13 +420,13 @@ def fused_reduce_rmsnorm_mxfp4(partials, residual: torch.Tensor | None, gamma: t
         y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     q = torch.empty((T, H // 2), dtype=torch.uint8, device=dev) if q is None else q
     scales = torch.empty((T, H // 32), dtype=torch.uint8, device=dev) if scales is None else scales
-    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev)
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev, out=True)
     if y is not None:
-        _check_tensor(y, "y", torch.bfloat16, (T, H), dev)
-    _check_tensor(q, "q", torch.uint8, (T, H // 2), dev)
-    _check_tensor(scales, "scales", torch.uint8, (T, H // 32), dev)
+        _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
+    _check_tensor(q, "q", torch.uint8, (T, H // 2), dev, out=True)
+    _check_tensor(scales, "scales", torch.uint8, (T, H // 32), dev, out=True)
     arr = (ctypes.c_void_p * R)(*ptrs)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = library().fused_reduce_rmsnorm_mxfp4(arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y),
                                                   _ptr(q), _ptr(scales), T, H, float(eps), _stream(stream, dev))
     _check(st)

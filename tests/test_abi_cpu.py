@@ -118,3 +118,14 @@ def test_no_device_maps_to_cuda_error(lib):
     st = _call(lib)
     assert st == frn.FRN_ERR_CUDA, frn.status_string(st)
     assert "cuda" in lib.frn_last_error_detail().decode().lower()
+
+
+def test_binding_rejects_host_inputs():
+    """Inputs must be CUDA tensors: the binding refuses host tensors before any
+    library call (no CPU fallback)."""
+    p = torch.zeros((2, 4, 256), dtype=torch.bfloat16)
+    g = torch.ones((256,), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="must be on"):
+        frn.fused_reduce_rmsnorm(p, None, g, 1e-6)
+    with pytest.raises(ValueError, match="must be on"):
+        frn.fused_reduce_rmsnorm_quant_per_group(p, None, g, 1e-6)

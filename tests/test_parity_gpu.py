@@ -242,6 +242,31 @@ def test_empty_T_is_noop():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("kernel", [frn.KERNEL_ROWS, frn.KERNEL_STREAM])
+def test_outputs_in_pinned_host_memory(kernel):
+    """Outputs may live in pinned host memory (the kernel writes them over the
+    host link): the same bits as device outputs."""
+    inp = syn.make_inputs(4, 37, 4096, seed=9, partial_std=0.5)
+    d = DevInputs(inp)
+    T, H = 37, 4096
+    pin = lambda dt, shape: torch.empty(shape, dtype=dt).pin_memory()
+    frn.set_kernel(kernel)
+    try:
+        ro_h, y_h = pin(torch.bfloat16, (T, H)), pin(torch.bfloat16, (T, H))
+        frn.fused_reduce_rmsnorm(d.partials, d.residual, d.gamma, d.eps, residual_out=ro_h, y=y_h)
+        q_h, s_h = pin(torch.float8_e4m3fn, (T, H)), pin(torch.float32, (T, H // 128))
+        ro2_h, y2_h = pin(torch.bfloat16, (T, H)), pin(torch.bfloat16, (T, H))
+        frn.fused_reduce_rmsnorm_quant_per_group(d.partials, d.residual, d.gamma, d.eps, 128, True,
+                                                 residual_out=ro2_h, y=y2_h, q=q_h, scales=s_h)
+        torch.cuda.synchronize()
+        ro_d, y_d = gpu_norm(d)
+        ro2_d, y2_d, q_d, s_d = gpu_quant(d, True)
+    finally:
+        frn.set_kernel(frn.KERNEL_AUTO)
+    for h, dv in ((ro_h, ro_d), (y_h, y_d), (ro2_h, ro2_d), (y2_h, y2_d), (q_h, q_d), (s_h, s_d)):
+        assert np.array_equal(host_bits(h).view(np.uint8), np.asarray(dv).view(np.uint8))
+
+
 def test_in_place_residual():
     inp = syn.make_inputs(4, 19, 4096, seed=3)
     d = DevInputs(inp)
