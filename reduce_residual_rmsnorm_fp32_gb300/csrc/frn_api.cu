@@ -107,7 +107,7 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
-frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
+frn::RowPlan choose_rows(long long T, int H, int R) {
     const int nvec = H / frn::kVecElems;
     const int ntiles = ceil_div(nvec, frn::kTileVecs);
     const int cmin = ceil_div(ntiles, frn::kMaxTilesPerCta);
@@ -388,7 +388,7 @@ bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms)
 
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
@@ -479,7 +479,7 @@ frn_status run_unfused(Call c, int stages, frn_stream_t stream) {
                          : reinterpret_cast<uint4*>(ws + (need_x ? 4LL * c.T * c.H : 0));
     Call norm = c;
     norm.y = ytarget;
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     frn::Params p = make_params(norm, rplan, splan, nullptr);
     cudaError_t e = cudaSuccess;
@@ -703,7 +703,7 @@ FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* 
         if (threads_per_cta) *threads_per_cta = (plan.groups * plan.consumer_warps + 1) * 32;
         if (grid_ctas) *grid_ctas = plan.grid;
     } else {
-        const frn::RowPlan plan = choose_rows(T, H, R, sms);
+        const frn::RowPlan plan = choose_rows(T, H, R);
         if (ctas_per_row) *ctas_per_row = plan.ctas_per_row;
         if (threads_per_cta) *threads_per_cta = plan.threads;
         if (grid_ctas) *grid_ctas = plan.grid;
