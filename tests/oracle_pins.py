@@ -409,6 +409,23 @@ def pin_mxfp4_all_zero_block(o):
     assert sc[0, 1] == -1 - 2 + 127 and ((q[0, 20] & 0xF) == 0x7)   # 0.75 / 2^-3 = 6
 
 
+def pin_mxfp4_clamped_exponent(o):
+    """A block of bf16 subnormals: floor(log2(absmax)) - 2 falls below E8M0's
+    -127, so the scale code is 0 (2^-127) and the elements are y * 2^127:
+    2^-130 becomes 0.125 -> 0 (nearest), 2^-129 becomes 0.25 -> 0 (the tie
+    between 0 and 0.5 goes to the even code), 3 * 2^-130 becomes 0.375 -> 0.5."""
+    y = np.zeros((1, 32), np.uint16)
+    y[0, 0] = 0x0008          # 2^-130 (bf16 subnormal: 8 * 2^-133)
+    y[0, 1] = 0x0010          # 2^-129
+    y[0, 2] = 0x0018          # 3 * 2^-130
+    y[0, 5] = 0x8018          # -3 * 2^-130
+    q, sc = o.mxfp4(y)
+    bq, bsc = bf.mxfp4(y)
+    assert sc[0, 0] == 0 and bsc[0, 0] == 0
+    assert np.array_equal(q, bq)
+    assert (q[0, 0] & 0xF) == 0x0 and (q[0, 0] >> 4) == 0x0 and (q[0, 1] & 0xF) == 0x1 and (q[0, 2] >> 4) == 0x9
+
+
 def pin_mxfp4_bruteforce(o):
     """Exact shared exponent and exhaustive-search codes on random blocks."""
     rng = np.random.default_rng(52)

@@ -94,3 +94,17 @@ def test_mxfp4_rejects_bad_h():
     d = DevInputs(inp)
     with pytest.raises(ValueError):
         frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps)
+
+
+def test_mxfp4_subnormal_y(kernel):
+    """gamma among the bf16 subnormals makes y subnormal: the shared exponent
+    clamps at E8M0's -127 (scale code 0) and the elements are y * 2^127."""
+    inp = syn.make_inputs(2, 9, 2048, seed=12)
+    rng = np.random.default_rng(5)
+    g = rng.integers(1, 0x80, size=2048).astype(np.uint16)   # 1..127 * 2^-133
+    g[::7] |= 0x8000
+    inp = syn.Inputs(inp.partials, inp.residual, g, inp.eps)
+    check_mx(inp, f"mx subnormal y k={kernel}")
+    d = DevInputs(inp)
+    (q, s), _ = frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps)
+    assert np.all(host_bits(s) == 0)

@@ -267,6 +267,17 @@ def test_outputs_in_pinned_host_memory(kernel):
         assert np.array_equal(host_bits(h).view(np.uint8), np.asarray(dv).view(np.uint8))
 
 
+def test_quant_subnormal_y(kernel):
+    """gamma among the bf16 subnormals makes y and absmax/448 tiny (fp32
+    subnormal scales): the kernels take the IEEE divides there and match the
+    oracle's codes and scales."""
+    inp = syn.make_inputs(2, 9, 2048, seed=13)
+    rng = np.random.default_rng(6)
+    g = rng.integers(1, 0x80, size=2048).astype(np.uint16)
+    g[::5] |= 0x8000
+    check_quant(syn.Inputs(inp.partials, inp.residual, g, inp.eps), f"quant subnormal y kernel={kernel}")
+
+
 def test_in_place_residual():
     inp = syn.make_inputs(4, 19, 4096, seed=3)
     d = DevInputs(inp)
