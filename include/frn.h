@@ -309,9 +309,10 @@ frn_status frn_device_status(int clear);
 
 /*
  * Test hook for the failure path above.  inject_stall != 0 makes every CTA of
- * the stream kernel skip its first bulk copy, so that the consumers' wait on it
- * runs out; wait_limit_ns > 0 replaces the 2 s bound (<= 0 restores it).  The
- * kernel then returns with the status word set and the context stays usable.
+ * the stream kernel skip its first bulk copy, and the row kernel's cluster
+ * shape never push tile 0's sum, so that the waits on them run out;
+ * wait_limit_ns > 0 replaces the 2 s bound (<= 0 restores it).  The kernel then
+ * returns with the status word set and the context stays usable.
  */
 frn_status frn_set_test_hooks(int inject_stall, int64_t wait_limit_ns);
 

@@ -77,7 +77,8 @@ struct Params {
     int slots;               // shared-memory ring slots, one row slice (2*H bytes) each
     int slice_bytes;
     unsigned long long wait_limit_ns;   // bound on every mbarrier wait
-    int inject_stall;        // test hook: never issue the first copy (forces a timeout)
+    int inject_stall;        // test hook: stream kernel never issues its first copy, cluster rows
+                             // never push tile 0's sum (either forces a bounded wait to run out)
     unsigned int* error_word;           // device status word, set on a timed-out wait
 };
 

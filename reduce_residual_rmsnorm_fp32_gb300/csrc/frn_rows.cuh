@@ -127,7 +127,8 @@ frn_row_kernel(const __grid_constant__ Params p) {
     float lo, hi;   // tile slots `lane` and `lane + 32` of the row
     if constexpr (CLUSTER) {
         cluster_wait_acquire();   // every CTA of the cluster has armed its row barrier
-        if (tile < p.ntiles && lane < p.ctas_per_row)
+        // (test hook: tile 0's sum is never pushed, so every CTA's wait runs out)
+        if (tile < p.ntiles && lane < p.ctas_per_row && !(p.inject_stall && tile == 0))
             st_async_f32(cluster_addr(&tile_sum[tile], static_cast<uint32_t>(lane)), s,
                          cluster_addr(&row_bar, static_cast<uint32_t>(lane)));
         if (!mbar_wait_bounded(smem_addr(&row_bar), 0u, p.wait_limit_ns) && lane == 0 && p.error_word)
