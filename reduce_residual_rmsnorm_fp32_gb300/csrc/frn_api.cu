@@ -100,6 +100,7 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
     frn::RowPlan plan;
     plan.ctas_per_row = 1;
     plan.tiles_per_cta = ntiles;
+    plan.rows_per_cta = 1;
     plan.threads = ntiles * 32;
     plan.grid = T;
     return plan;
@@ -107,7 +108,7 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
-frn::RowPlan choose_rows(long long T, int H, int R) {
+frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     const int nvec = H / frn::kVecElems;
     const int ntiles = ceil_div(nvec, frn::kTileVecs);
     const int cmin = ceil_div(ntiles, frn::kMaxTilesPerCta);
@@ -154,8 +155,13 @@ frn::RowPlan choose_rows(long long T, int H, int R) {
     frn::RowPlan plan;
     plan.ctas_per_row = C;
     plan.tiles_per_cta = tpc;
-    plan.threads = tpc * 32;
-    plan.grid = T * C;
+    plan.rows_per_cta = 1;
+    // Short rows (<= 4 tiles, H <= 1024) with several rows per SM: 256-thread
+    // CTAs of 8 / ntiles consecutive rows, instead of CTAs of one to four
+    // warps (an SM holds at most 32 CTAs).
+    if (C == 1 && ntiles <= 4 && T >= 4LL * num_sms) plan.rows_per_cta = 8 / ntiles;
+    plan.threads = plan.rows_per_cta * tpc * 32;
+    plan.grid = (T + plan.rows_per_cta - 1) / plan.rows_per_cta * C;
     return plan;
 }
 
@@ -359,6 +365,7 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
     p.nvec = c.H / frn::kVecElems;
     p.ntiles = ceil_div(p.nvec, frn::kTileVecs);
     p.tiles_per_cta = rplan.tiles_per_cta;
+    p.rows_per_cta = rplan.rows_per_cta;
     p.ctas_per_row = rplan.ctas_per_row;
     p.eps = c.eps;
     p.nslices = c.R + (c.residual ? 1 : 0);
@@ -377,18 +384,21 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // when it is not NULL.
 // The L2 prefetch pays when the grid is at most about two waves (most CTAs
 // start while the previous kernel on the stream drains, or while the first
-// wave runs), and each CTA loads at least 48 KB or the grid has at least 64
-// CTAs (measured: below both, the extra requests cost more than the overlap
-// gives; beyond two waves it gains nothing).
+// wave runs) and there is enough to fetch: a single-CTA row of at least 32 KB
+// of loads, or a cluster CTA of at least 48 KB or a grid of at least 64
+// cluster CTAs.  Measured on GB300: below that, and for packed short rows
+// (up to 2x slower at H = 256), the extra requests cost more than the overlap
+// gives; beyond two waves it gains nothing.
 bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms) {
-    if (plan.grid * plan.threads > 2048LL * sms) return false;
-    const long long cta_bytes = 2LL * H * (R + 1) / plan.ctas_per_row;
-    return cta_bytes >= 48 * 1024 || T * plan.ctas_per_row >= 64;
+    if (plan.grid * plan.threads > 2048LL * sms || plan.rows_per_cta > 1) return false;
+    const long long row_bytes = 2LL * H * (R + 1);
+    if (plan.ctas_per_row == 1) return row_bytes >= 32 * 1024;
+    return row_bytes / plan.ctas_per_row >= 48 * 1024 || T * plan.ctas_per_row >= 64;
 }
 
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
@@ -411,7 +421,8 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // T = 8192 (issue-bound there), so it is left out for those beyond four
     // waves; with R >= 4 it cost 8..17% (enough loads in flight already).
     if (kind == kRows && pf != 1 && c.R <= 2) {
-        const long long wave_rows = static_cast<long long>(2048 / rplan.threads) * sms / rplan.ctas_per_row;
+        const long long wave_rows =
+            static_cast<long long>(2048 / rplan.threads) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
         const bool yless_quant = quant == 1 || quant == 3;
         if (wave_rows > 0 && c.T > wave_rows && (!yless_quant || c.T <= 4 * wave_rows))
             p.prefetch_ahead = wave_rows;
@@ -479,7 +490,7 @@ frn_status run_unfused(Call c, int stages, frn_stream_t stream) {
                          : reinterpret_cast<uint4*>(ws + (need_x ? 4LL * c.T * c.H : 0));
     Call norm = c;
     norm.y = ytarget;
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     frn::Params p = make_params(norm, rplan, splan, nullptr);
     cudaError_t e = cudaSuccess;
@@ -703,7 +714,7 @@ FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* 
         if (threads_per_cta) *threads_per_cta = (plan.groups * plan.consumer_warps + 1) * 32;
         if (grid_ctas) *grid_ctas = plan.grid;
     } else {
-        const frn::RowPlan plan = choose_rows(T, H, R);
+        const frn::RowPlan plan = choose_rows(T, H, R, sms);
         if (ctas_per_row) *ctas_per_row = plan.ctas_per_row;
         if (threads_per_cta) *threads_per_cta = plan.threads;
         if (grid_ctas) *grid_ctas = plan.grid;

@@ -48,15 +48,20 @@ __device__ __forceinline__ void prefetch_tile_span(const Params& p, long long ro
 // the prefill shapes live on that), R <= 4 at 40 (three 512-thread rows),
 // R <= 8 at 64.  Cluster rows (H > 8192, or a few heavy decode rows) keep
 // what the compiler picks.
+constexpr int kPackedThreads = 256;   // the packed short-row variant
+
 constexpr int row_min_blocks(int rmax, bool cluster, int maxt) {
     return cluster ? 1
          : maxt > kMaxThreads ? (rmax <= 2 ? 2 : 1)
-                              : (rmax <= 2 ? 4 : rmax <= 4 ? 3 : rmax <= 8 ? 2 : 1);
+         : maxt == kPackedThreads ? (rmax <= 2 ? 8 : rmax <= 4 ? 6 : rmax <= 8 ? 4 : 2)
+                                  : (rmax <= 2 ? 4 : rmax <= 4 ? 3 : rmax <= 8 ? 2 : 1);
 }
 
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
 __global__ void __launch_bounds__(MAXT, row_min_blocks(RMAX, CLUSTER, MAXT))
 frn_row_kernel(const __grid_constant__ Params p) {
+    // MAXT == 256 (single CTA only): several short rows per CTA, ntiles warps each
+    constexpr bool kPacked = !CLUSTER && MAXT == kPackedThreads;
     // single CTA: this CTA's tile sums; cluster: every tile sum of the row
     __shared__ float tile_sum[CLUSTER ? kMaxTiles : MAXT / 32];
     __shared__ __align__(8) uint64_t row_bar;   // cluster: counts the pushed tile sums
@@ -64,16 +69,21 @@ frn_row_kernel(const __grid_constant__ Params p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int rank = 0;
+    int rsub = 0;        // packed short rows: which of the CTA's rows_per_cta rows this warp works on
     long long row;
     if constexpr (CLUSTER) {
         rank = static_cast<int>(cluster_ctarank());
         row = blockIdx.x / p.ctas_per_row;
+    } else if constexpr (kPacked) {
+        rsub = warp / p.tiles_per_cta;
+        row = static_cast<long long>(blockIdx.x) * p.rows_per_cta + rsub;
     } else {
         row = blockIdx.x;
     }
-    const int tile = rank * p.tiles_per_cta + warp;
+    const int tile = rank * p.tiles_per_cta + (warp - rsub * p.tiles_per_cta);
     const int j = tile * kTileVecs + lane;              // vector index in the row
-    const bool valid = j < p.nvec;
+    const bool in_rows = !kPacked || row < p.T;         // the last packed CTA's rows may end early
+    const bool valid = j < p.nvec && in_rows;
     const long long off = row * static_cast<long long>(p.nvec) + j;
 
     if constexpr (CLUSTER) {
@@ -94,7 +104,7 @@ frn_row_kernel(const __grid_constant__ Params p) {
     // finishing.  A prefetch hands no value to this kernel, and L2 is where the
     // previous kernel's writes land, so every value read after the wait below
     // is still the completed one.
-    if (p.prefetch_l2 && tile < p.ntiles) prefetch_tile_span(p, row, tile, lane, true);
+    if (p.prefetch_l2 && tile < p.ntiles && in_rows) prefetch_tile_span(p, row, tile, lane, true);
     // Many rows: ask for the same tile of the row about one wave of CTAs ahead,
     // so that the CTA which takes that row finds it in L2.
     if (p.prefetch_ahead > 0 && tile < p.ntiles && row + p.prefetch_ahead < p.T)
@@ -136,24 +146,27 @@ frn_row_kernel(const __grid_constant__ Params p) {
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
         hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     } else {
+        // this CTA's rows are consecutive groups of ntiles warps
         if (lane == 0) tile_sum[warp] = s;
         __syncthreads();
-        lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
-        hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
+        const float* ts = tile_sum + rsub * p.tiles_per_cta;
+        lo = lane < p.ntiles ? ts[lane] : 0.0f;
+        hi = lane + 32 < p.ntiles ? ts[lane + 32] : 0.0f;
     }
     float rstd;
     if (!CLUSTER && p.rstd_one_warp) {
-        // Many rows: warp 0 alone finishes the reduction and hands rstd to the
-        // others through shared memory -- one more barrier, but the butterfly,
-        // divide and square root leave every other warp's issue slots free for
-        // the CTAs that share the SM.  Same tree, same bits.
-        __shared__ float rstd_sh;
-        if (warp == 0) {
+        // Many rows: the first warp of each row alone finishes the reduction
+        // and hands rstd to the others through shared memory -- one more
+        // barrier, but the butterfly, divide and square root leave every other
+        // warp's issue slots free for the CTAs that share the SM.  Same tree,
+        // same bits.
+        __shared__ float rstd_sh[CLUSTER ? 1 : MAXT / 32];
+        if (warp == rsub * p.tiles_per_cta) {
             const float r0 = row_rstd(lo, hi, p.H, p.eps);
-            if (lane == 0) rstd_sh = r0;
+            if (lane == 0) rstd_sh[rsub] = r0;
         }
         __syncthreads();
-        rstd = rstd_sh;
+        rstd = rstd_sh[rsub];
     } else {
         rstd = row_rstd(lo, hi, p.H, p.eps);
     }
@@ -195,6 +208,7 @@ frn_row_kernel(const __grid_constant__ Params p) {
 struct RowPlan {
     int ctas_per_row;
     int tiles_per_cta;
+    int rows_per_cta;   // single-CTA rows only: short rows share a CTA
     int threads;
     long long grid;
 };
@@ -249,6 +263,15 @@ cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t strea
         if (p.R <= 2) return launch_row_one<2, MODE, false, 1024>(p, plan, stream, pdl);
         if (p.R <= 4) return launch_row_one<4, MODE, false, 1024>(p, plan, stream, pdl);
         return launch_row_one<8, MODE, false, 1024>(p, plan, stream, pdl);
+    }
+    if (plan.rows_per_cta > 1) {
+        // several short rows per CTA (the host plans this for one CTA per row
+        // and at most kPackedThreads threads)
+        if (p.R <= 1) return launch_row_one<1, MODE, false, kPackedThreads>(p, plan, stream, pdl);
+        if (p.R <= 2) return launch_row_one<2, MODE, false, kPackedThreads>(p, plan, stream, pdl);
+        if (p.R <= 4) return launch_row_one<4, MODE, false, kPackedThreads>(p, plan, stream, pdl);
+        if (p.R <= 8) return launch_row_one<8, MODE, false, kPackedThreads>(p, plan, stream, pdl);
+        return launch_row_one<16, MODE, false, kPackedThreads>(p, plan, stream, pdl);
     }
     const bool cl = plan.ctas_per_row > 1;
 #define FRN_DISPATCH_R(RM)                                                        \

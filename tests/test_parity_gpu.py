@@ -208,6 +208,30 @@ def test_many_row_launches_are_bit_identical(R):
         assert np.array_equal(np.asarray(a)[:13].view(np.uint8), np.asarray(c).view(np.uint8))
 
 
+@pytest.mark.parametrize("H", [256, 512, 768, 1024])
+@pytest.mark.parametrize("R", [1, 2, 8])
+def test_packed_short_rows(H, R):
+    """Short rows at many T share 256-thread CTAs (8 / ntiles rows each, the
+    last CTA ragged): every row matches the oracle, and its bits are those of
+    a one-row-per-CTA call of the same rows."""
+    T = 613
+    inp = syn.make_inputs(R, T, H, seed=14 + H + R, partial_std=0.5)
+    kernel, ctas, threads, grid = frn.query_launch(T, H, R)
+    ntiles = -(-H // 256)
+    assert (kernel, ctas, threads, grid) == (frn.KERNEL_ROWS, 1, (8 // ntiles) * ntiles * 32,
+                                             -(-T // (8 // ntiles)))
+    if H % 128 == 0:
+        check_quant(inp, f"packed H={H} R={R}")
+    else:
+        check_norm(inp, f"packed H={H} R={R}")
+    d = DevInputs(inp)
+    ro, y = gpu_norm(d)
+    few = DevInputs(syn.Inputs(inp.partials[:, 600:], inp.residual[600:], inp.gamma, inp.eps))
+    assert frn.query_launch(13, H, R)[2] == ntiles * 32
+    ro_f, y_f = gpu_norm(few)
+    assert np.array_equal(ro[600:], ro_f) and np.array_equal(y[600:], y_f)
+
+
 @pytest.mark.parametrize("prefetch", [1, 2])
 @pytest.mark.parametrize("ctas", [1, 3, 8])
 @pytest.mark.parametrize("H", [7000, 16384, 2056])
