@@ -21,6 +21,11 @@ def test_fake_impls_give_shapes_without_a_gpu():
         assert y.shape == (0, 256) and q.dtype == torch.float8_e4m3fn and s.shape == (5, 2)
         y, q, s, ro = torch.ops.frn.fused_reduce_rmsnorm_quant_per_group(parts, res, g, 1e-6, 128, True)
         assert y.shape == (5, 256)
+        y, q, s, ro = torch.ops.frn.fused_reduce_rmsnorm_mxfp4(parts, res, g, 1e-6, False)
+        assert y.shape == (0, 256) and q.shape == (5, 128) and q.dtype == torch.uint8 and s.shape == (5, 8)
+        y, ro = torch.ops.frn.fused_add_rmsnorm(parts[0], res, g, 1e-6)
+        assert y.shape == (5, 256) and ro.shape == (5, 256)
+        assert torch.ops.frn.rmsnorm(parts[0], g, 1e-6).shape == (5, 256)
 
 
 @pytest.mark.gpu
@@ -50,3 +55,20 @@ def test_ops_match_binding_in_compile_and_graph():
     gr.replay()
     torch.cuda.synchronize()
     assert torch.equal(out[0], yg) and torch.equal(out[1], rog)
+
+
+@pytest.mark.gpu
+def test_mxfp4_and_adjacent_ops_match_binding():
+    import reduce_residual_rmsnorm_fp32_gb300 as frn
+    from frn_testlib import dev_bf16
+    inp = syn.make_inputs(2, 16, 2048, seed=4, partial_std=0.5)
+    parts = [dev_bf16(inp.partials[r]) for r in range(2)]
+    res, g = dev_bf16(inp.residual), dev_bf16(inp.gamma)
+    (yb, qb, sb), rob = frn.fused_reduce_rmsnorm_mxfp4(parts, res, g, inp.eps, True)
+    y, q, s, ro = torch.compile(lambda ps, r, gg: torch.ops.frn.fused_reduce_rmsnorm_mxfp4(ps, r, gg, 1e-6, True),
+                                fullgraph=True)(parts, res, g)
+    assert torch.equal(y, yb) and torch.equal(q, qb) and torch.equal(s, sb) and torch.equal(ro, rob)
+    ya, roa = frn.fused_add_rmsnorm(parts[0], res, g, inp.eps)
+    y2, ro2 = torch.ops.frn.fused_add_rmsnorm(parts[0], res, g, 1e-6)
+    assert torch.equal(y2, ya) and torch.equal(ro2, roa)
+    assert torch.equal(torch.ops.frn.rmsnorm(parts[0], g, 1e-6), frn.rmsnorm(parts[0], g, inp.eps))
