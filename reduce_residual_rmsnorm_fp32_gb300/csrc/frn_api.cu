@@ -178,7 +178,12 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
     frn::StreamPlan plan;
     plan.tiles_per_warp = tpw;
     plan.consumer_warps = ceil_div(ntiles, tpw);
-    const int max_warps = (tpw == 4 && nslices <= 4) ? frn::kStreamMaxThreads / 32 : 16;
+    int max_warps = (tpw == 4 && nslices <= 4) ? frn::kStreamMaxThreads / 32 : 16;
+    // a 17th warp (the 544-thread variant) when it buys a second group of 8 and
+    // rows have at most 5 slices (H = 8192, R = 4: 80 -> 75 us without quant,
+    // 114 -> 96 us with FP8 B; with R = 8 the single group's deeper sub-ring
+    // measured 5% faster without quant)
+    if (max_warps == 16 && plan.consumer_warps == 8 && nslices <= 5) max_warps = 17;
     int groups = g_force_groups.load(std::memory_order_relaxed);
     if (groups <= 0) groups = (max_warps - 1) / plan.consumer_warps;
     if (groups > frn::kStreamMaxGroups) groups = frn::kStreamMaxGroups;
@@ -197,12 +202,12 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
 // Which kernel (measured on GB300 at H = 7168, R = 1..8, T = 8..8192):
 //  * a row that fits one 512-thread CTA (H <= 4096): the row kernel at any T
 //    (several rows in flight per SM);
-//  * a row for a wide CTA (H <= 8192, R <= 8): the row kernel, except from
-//    2 rows per SM on with R != 2, where the stream kernel's overlap of one
-//    row's epilogue with the next rows' loads wins (with R = 2 the row kernel
-//    -- 32 registers, two rows per SM, one-wave-ahead L2 prefetch, rstd from
-//    one warp -- wins for every output variant; R = 3 unrolls as 4 and keeps
-//    one wide row per SM, 40% slower);
+//  * a row for a wide CTA (H <= 8192, R <= 8): the row kernel below 2 rows per
+//    SM; beyond, the row kernel when two of its wide CTAs fit on an SM (R <= 2
+//    up to H = 8192, R <= 4 up to H = 5440, every output variant: e.g. 47 vs
+//    55 us at R = 4, T = 4096, H = 5120), else the stream kernel, whose overlap
+//    of one row's epilogue with the next rows' loads then wins (R = 3..4 at
+//    H = 7168: 68 vs 81 us at T = 4096);
 //  * a wider row: the stream kernel from one row per SM on.
 int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     (void)quant;
@@ -212,7 +217,12 @@ int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     if (ntiles <= frn::kMaxTilesPerCta) return kRows;
     if (wide_possible(ntiles, R)) {
         if (T < 2LL * num_sms) return kRows;
-        return R == 2 ? kRows : kStream;
+        // two or more wide rows resident per SM (threads, and the registers the
+        // launch bound holds: 32 for R <= 2, 48 for R <= 4, 64 for R <= 8)
+        const int threads = ntiles * 32;
+        const int regs = R <= 2 ? 32 : (R <= 4 ? 48 : 64);
+        const int by_threads = 2048 / threads, by_regs = 65536 / (threads * regs);
+        return (by_threads < by_regs ? by_threads : by_regs) >= 2 ? kRows : kStream;
     }
     return T >= num_sms ? kStream : kRows;
 }
