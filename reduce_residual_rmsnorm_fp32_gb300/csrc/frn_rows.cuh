@@ -1,10 +1,12 @@
 // frn_rows.cuh -- the row kernel: one token row per CTA or per thread-block
-// cluster.
+// cluster, or several short rows per CTA.
 //
 // The tiles of a row go to one CTA (up to 1024 threads) or are spread over C
 // CTAs of one cluster (tiles_per_cta warps each, one tile per warp): a row too
 // wide for one CTA, or one of a few heavy decode rows, so that a handful of
-// tokens still spreads over several SMs.  Every thread issues all of its R+1
+// tokens still spreads over several SMs.  Rows of at most 4 tiles, when there
+// are many, share 256-thread CTAs (the MAXT == 256 instantiation), 8 / ntiles
+// consecutive rows each.  Every thread issues all of its R+1
 // 128-bit loads (partials through the read-only path, no L1 allocation,
 // 256-byte L2 prefetch) before its first add, so each byte of HBM is read
 // exactly once and the row stays in registers until y is written.
@@ -41,8 +43,9 @@ __device__ __forceinline__ void prefetch_tile_span(const Params& p, long long ro
 
 // RMAX is the unrolled partial count (R <= RMAX; loads beyond R are predicated
 // off).  CLUSTER == false is the single-CTA row (no cluster barriers).  MAXT is
-// the launch bound: 512 threads (16 tiles), or 1024 for a single-CTA row of up
-// to 32 tiles (H <= 8192, R <= 8: 64 registers a thread).  The second bound
+// the launch bound: 512 threads (16 tiles), 1024 for a single-CTA row of up
+// to 32 tiles (H <= 8192, R <= 8: 64 registers a thread), or 256 for packed
+// short rows (R <= 2 at 32 registers, R <= 4 at 40, R <= 8 at 64).  The second bound
 // holds the register count of a single-CTA row where the row count per SM
 // needs it: R <= 2 at 32 registers (two wide or four 512-thread rows per SM:
 // the prefill shapes live on that), R <= 4 at 40 (three 512-thread rows),
