@@ -45,6 +45,11 @@ MUTANTS = {
     "e2m1_no_saturation": [("if (r > 6.0) r = 6.0;", "")],
     "e2m1_subnormal_wrong": [("if (r < 1.0) return sign | 0x1;", "if (r < 1.0) return sign;")],
     "mx_nibble_order_swapped": [("qb[i] = (uint8_t)(lo | (hi << 4));", "qb[i] = (uint8_t)(hi | (lo << 4));")],
+    "mx_no_lower_clamp": [("if (shared_exp < -127) shared_exp = -127;", "")],
+    "mx_zero_block_code_one": [("int shared_exp = -127;", "int shared_exp = 0;")],
+    "mx_scale_rounds_log2": [("(void)frexp(amax, &ex);", "(void)frexp(amax * 1.4142135623730951, &ex);")],
+    "mx_divides_by_amax": [("ldexp(oracle_bf16_to_double(yb[2 * i]), -shared_exp)",
+                            "oracle_bf16_to_double(yb[2 * i]) / amax * 6.0")],
 }
 
 
