@@ -302,15 +302,17 @@ def test_quant_subnormal_y(kernel):
     check_quant(syn.Inputs(inp.partials, inp.residual, g, inp.eps), f"quant subnormal y kernel={kernel}")
 
 
-def test_in_place_residual():
-    inp = syn.make_inputs(4, 19, 4096, seed=3)
+@pytest.mark.parametrize("T,H", [(19, 4096), (700, 512), (300, 7168)])
+def test_in_place_residual(T, H, kernel):
+    """residual_out == residual (in place), for every kernel and row shape."""
+    inp = syn.make_inputs(4, T, H, seed=3)
     d = DevInputs(inp)
     rro, ry = ref_norm(inp)
     res = d.residual.clone()
     y, ro = frn.fused_reduce_rmsnorm(d.partials, res, d.gamma, inp.eps, residual_out=res)
     assert ro.data_ptr() == res.data_ptr()
-    assert_residual_exact(host_bits(res), rro, "in place")
-    assert_y_close(host_bits(y), ry, "in place")
+    assert_residual_exact(host_bits(res), rro, f"in place T={T} H={H} kernel={kernel}")
+    assert_y_close(host_bits(y), ry, f"in place T={T} H={H} kernel={kernel}")
 
 
 def test_separate_partial_allocations_and_repeats():
