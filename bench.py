@@ -7,21 +7,27 @@ is effective GB/s -- algorithmic HBM bytes of the step over its device time --
 next to its fraction of the measured HBM peak, plus microseconds per call at
 each decode T.  Each step reads a different one of several rotating input
 sets whose total size exceeds twice the L2, so no step hits inputs the previous
-one left in L2.  Steps run as CUDA-graph replays (one graph per input set, four
-launches each), as a decode engine records them.
+one left in L2.  Steps run as CUDA-graph replays: one graph holds one step per
+input set (four launches each), as a decode engine's graph holds the epilogues
+of all its layers.
 
 Besides the JSON contract keys, the line carries:
   decode_us_per_call  per T: graph replay and raw (Python-launched) calls
   large_T             the >= 1024-token workloads: the message sweep at
                       16/32/64 MB per partial and the 8192-token prefill chunk
-                      with per-group FP8 quant (both output variants), each with
-                      effective GB/s and fraction of HBM peak
+                      with per-group FP8 quant (both output variants), without
+                      quant and with MXFP4, each with effective GB/s and
+                      fraction of HBM peak
   sweep               all 12 message sizes, 32 KB .. 64 MB per partial
+  quant_R4_T32_H4096  the FP8 workload R=4, T=32, H=4096, both output variants
+  fusion_gain         the fused call against the 2- and 3-kernel unfused paths
   roofline            the dominant kernel of the step (the T=64 call)
   cpu_baseline        the CPU oracle on this host's cores, on a bounded sample
-  e2e                 the step through the public API with pinned host buffers,
-                      host->device copies of the inputs and device->host reads
-                      of the outputs inside the timed region
+                      (and on one thread)
+  e2e                 the step through the public API with pinned host buffers:
+                      the host->device copy of the inputs and the kernels'
+                      writes of the outputs into pinned host memory inside the
+                      timed region
 
 ``--impl reference`` times the CPU oracle (the reference arm) on the same
 workload and metric instead.  Under torchrun every rank runs its own replica of
