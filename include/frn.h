@@ -23,7 +23,8 @@
  *    (AITER PR 4346), "Pull request overview": a fused call must never read a
  *    partial before its producer has finished, nor let the next call reuse
  *    buffers the previous one still reads.  Here that is stream order: every
- *    kernel starts with a grid-dependency wait before its first global access.
+ *    kernel waits on the previous grid before its first global load or store
+ *    (only L2 prefetch hints, which hand no value to the kernel, come first).
  *
  * Per token row t, with f32() the exact bf16 -> fp32 widening:
  *   x_hat        = ((f32(P0[t]) + f32(P1[t])) + ... + f32(P[R-1][t])) + f32(residual[t])
@@ -259,19 +260,21 @@ int frn_version(void);
  *   first global-memory load or store (only an L2 prefetch hint, which hands
  *   no value to the kernel, may precede the wait).  0 launches plainly.
  * frn_set_kernel: 0 (default) picks the kernel from T, H and the SM count;
- *   1 forces the row kernel (one row per thread-block cluster, for few rows),
+ *   1 forces the row kernel (a row per CTA, wide CTA or thread-block cluster,
+ *   or several short rows per CTA; registers hold each row),
  *   2 forces the stream kernel (persistent, one CTA per SM, rows streamed
  *   through shared memory with TMA bulk copies, for many rows).
  * frn_set_ctas_per_row: row kernel only.  0 (default) chooses from T, H, R
- *   and the SM count between one CTA per row and a cluster of CTAs per row;
+ *   and the SM count between one CTA per row (several short rows per CTA when
+ *   H <= 1024 and T is large) and a cluster of CTAs per row;
  *   1 forces one CTA per row (up to 1024 threads when H <= 8192 and R <= 8,
  *   else the smallest cluster that holds the row); 2..16 force a cluster of
  *   that many CTAs (rounded so that no CTA is empty; 9..16 is a non-portable
  *   cluster size, with at least two tiles a CTA).
  * frn_set_stream_groups: stream kernel only.  0 (default) chooses how many
  *   consumer groups (each taking every n-th row of a CTA, so that one group's
- *   epilogue overlaps the next group's loads) from H; 1..4 forces it, reduced
- *   where the CTA would exceed 16 warps.
+ *   epilogue overlaps the next group's loads) from H and the slices a row
+ *   has; 1..4 forces it, reduced where the CTA would exceed its warp budget.
  * frn_set_l2_prefetch: row kernel only.  0 (default) decides from the launch
  *   shape whether each warp asks for its slice of the row to be fetched into
  *   L2 before the wait on the previous kernel, and, for grids of more than
