@@ -289,6 +289,40 @@ frn_status frn_set_ctas_per_row(int ctas_per_row);
 frn_status frn_set_stream_groups(int groups);
 
 /*
+ * The launch the library plans for a call of these sizes on a device with
+ * num_sms SMs, without touching a device (host code only; for inspection and
+ * tests).  quant as for frn_query_launch; has_residual != 0 when a residual
+ * is passed (the stream kernel then streams R + 1 slices a row).  T >= 1.
+ *   kernel          1 row kernel, 2 stream kernel
+ *   ctas_per_row    row kernel: CTAs of the row's cluster (1: one CTA)
+ *   rows_per_cta    row kernel: consecutive short rows a CTA (1 otherwise)
+ *   tiles_per_cta   row kernel: warps (32-vector tiles) a row has in a CTA
+ *   tiles_per_warp  stream kernel: tiles a consumer warp holds (row kernel 1)
+ *   threads, grid   threads per CTA, CTAs in the grid
+ *   groups, consumer_warps, slots, smem_bytes
+ *                   stream kernel: consumer groups, warps a group, ring slots
+ *                   (one 2*H-byte row slice each), dynamic shared memory
+ * Launch controls (frn_set_kernel, frn_set_ctas_per_row, ...) apply as they
+ * would to a call.
+ */
+typedef struct frn_launch_plan {
+    int kernel;
+    int ctas_per_row;
+    int rows_per_cta;
+    int tiles_per_cta;
+    int tiles_per_warp;
+    int threads;
+    int64_t grid;
+    int groups;
+    int consumer_warps;
+    int slots;
+    int smem_bytes;
+} frn_launch_plan;
+
+frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int has_residual, int num_sms,
+                           frn_launch_plan* out);
+
+/*
  * Report the launch a call with these sizes would use on the current device:
  * kernel (1 row, 2 stream), CTAs per row (cluster size; 1 for the stream
  * kernel and for a single wide CTA), threads per CTA, and CTAs in the grid.

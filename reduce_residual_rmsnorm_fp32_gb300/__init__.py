@@ -81,6 +81,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_set_kernel.restype = i32
     lib.frn_set_stream_groups.argtypes = [i32]
     lib.frn_set_stream_groups.restype = i32
+    lib.frn_plan_launch.argtypes = [i64, i32, i32, i32, i32, i32, vp]
+    lib.frn_plan_launch.restype = i32
     lib.frn_query_launch.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                      ctypes.POINTER(i32), ctypes.POINTER(i64)]
     lib.frn_query_launch.restype = i32
@@ -153,6 +155,22 @@ def set_kernel(kind: int) -> None:
 def set_stream_groups(groups: int) -> None:
     """Stream kernel consumer groups: 0 = automatic, 1..4 forced."""
     _check(library().frn_set_stream_groups(int(groups)))
+
+
+class _LaunchPlan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("ctas_per_row", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
+                ("tiles_per_cta", ctypes.c_int), ("tiles_per_warp", ctypes.c_int), ("threads", ctypes.c_int),
+                ("grid", ctypes.c_int64), ("groups", ctypes.c_int), ("consumer_warps", ctypes.c_int),
+                ("slots", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+
+
+def plan_launch(T: int, H: int, R: int, quant: int = 0, residual: bool = True, num_sms: int = 152) -> dict:
+    """The launch the library plans for these sizes on a device with num_sms SMs
+    (host code only: no device is touched).  See frn_plan_launch in frn.h."""
+    out = _LaunchPlan()
+    _check(library().frn_plan_launch(int(T), int(H), int(R), int(quant), 1 if residual else 0, int(num_sms),
+                                     ctypes.byref(out)))
+    return {name: getattr(out, name) for name, _ in _LaunchPlan._fields_}
 
 
 def query_launch(T: int, H: int, R: int, quant: int = 0) -> tuple[int, int, int, int]:

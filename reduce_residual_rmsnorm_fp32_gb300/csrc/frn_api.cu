@@ -709,6 +709,37 @@ FRN_EXPORT frn_status frn_device_status(int clear) {
     return ok();
 }
 
+FRN_EXPORT frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int has_residual, int num_sms,
+                                      frn_launch_plan* out) {
+    if (R < 1 || R > FRN_MAX_PARTIALS || T < 1 || H < 8 || H % 8 != 0 || H > FRN_MAX_HIDDEN || quant < 0 ||
+        quant > 4 || num_sms < 1 || !out)
+        return fail(FRN_ERR_INVALID_ARG, "bad sizes");
+    std::memset(out, 0, sizeof(*out));
+    const int kind = choose_kind(T, H, R, quant, num_sms);
+    out->kernel = kind;
+    if (kind == kStream) {
+        const frn::StreamPlan plan = choose_stream(T, H, R + (has_residual ? 1 : 0), num_sms);
+        out->ctas_per_row = 1;
+        out->rows_per_cta = 1;
+        out->tiles_per_warp = plan.tiles_per_warp;
+        out->groups = plan.groups;
+        out->consumer_warps = plan.consumer_warps;
+        out->slots = plan.slots;
+        out->smem_bytes = plan.smem_bytes;
+        out->threads = (plan.groups * plan.consumer_warps + 1) * 32;
+        out->grid = plan.grid;
+    } else {
+        const frn::RowPlan plan = choose_rows(T, H, R, num_sms);
+        out->ctas_per_row = plan.ctas_per_row;
+        out->rows_per_cta = plan.rows_per_cta;
+        out->tiles_per_warp = 1;
+        out->tiles_per_cta = plan.tiles_per_cta;
+        out->threads = plan.threads;
+        out->grid = plan.grid;
+    }
+    return ok();
+}
+
 FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int* ctas_per_row,
                                        int* threads_per_cta, int64_t* grid_ctas) {
     if (R < 1 || T < 0 || H < 8 || H % 8 != 0 || H > FRN_MAX_HIDDEN || quant < 0 || quant > 4)

@@ -1,0 +1,111 @@
+"""The launch planner's shapes, checked on the CPU for every hidden size.
+
+frn_plan_launch runs the library's own kernel and launch-shape choice for a
+given SM count without touching a device.  Every plan must fit the kernel
+variant it selects: tiles covered with no empty CTA, thread counts within the
+launch bounds of the instantiation the dispatcher picks, shared memory within
+the opt-in limit, grids as the kernels index them."""
+import itertools
+
+import pytest
+
+import reduce_residual_rmsnorm_fp32_gb300 as frn
+from reduce_residual_rmsnorm_fp32_gb300 import _build
+
+SMEM_LIMIT = 232448
+TS = (1, 3, 8, 16, 33, 64, 127, 300, 608, 1171, 8192, 65536)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    return frn.library()
+
+
+def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
+    ntiles = -(-(H // 8) // 32)
+    what = (T, H, R, quant, residual, sms, pl)
+    if auto and ntiles <= 16:
+        assert pl["kernel"] == frn.KERNEL_ROWS, what
+    if pl["kernel"] == frn.KERNEL_ROWS:
+        C, tpc, rows, thr = pl["ctas_per_row"], pl["tiles_per_cta"], pl["rows_per_cta"], pl["threads"]
+        assert 1 <= C <= 16 and tpc >= 1 and rows >= 1, what
+        assert C * tpc >= ntiles and (C - 1) * tpc < ntiles, what          # every tile, no empty CTA
+        assert thr == rows * tpc * 32 and thr <= 1024, what
+        assert tpc <= 32, what                                             # per-CTA tile-sum slots
+        if rows > 1:                                                       # packed 256-thread variant
+            assert C == 1 and tpc == ntiles and thr <= 256, what
+        if thr > 512:                                                      # wide variant: one CTA, R <= 8
+            assert C == 1 and rows == 1 and R <= 8, what
+        if C > 1:                                                          # cluster variant: <= 512 threads
+            assert thr <= 512 and rows == 1 and C <= 8, what
+        assert pl["grid"] == -(-T // rows) * C, what
+    else:
+        tpw, nc, g, slots = pl["tiles_per_warp"], pl["consumer_warps"], pl["groups"], pl["slots"]
+        nslices = R + (1 if residual else 0)
+        assert tpw in (1, 2, 4) and nc * tpw >= ntiles and (nc - 1) * tpw < ntiles, what
+        assert 1 <= g <= 4 and pl["threads"] == (g * nc + 1) * 32 <= 704, what
+        if pl["threads"] > 512:                                            # 544 / 704 variants are TPW 4
+            assert tpw == 4, what
+        assert g <= slots <= 32 and slots * 2 * H <= pl["smem_bytes"] <= SMEM_LIMIT, what
+        assert pl["grid"] == min(T, sms), what
+        assert nslices >= 1, what
+
+
+def test_every_hidden_size_plans_a_valid_launch():
+    n = 0
+    for H in range(8, 16385, 8):
+        for R, T in itertools.product((1, 2, 3, 4, 8, 16), TS):
+            quants = [0] + ([1, 2] if H % 128 == 0 else []) + ([3, 4] if H % 32 == 0 else [])
+            for quant in quants:
+                for residual in (True, False):
+                    if quant and not residual and H % 512:
+                        continue   # thin the sample: residual-free quant on a quarter of H
+                    pl = frn.plan_launch(T, H, R, quant, residual, 152)
+                    _check_plan(pl, T, H, R, quant, residual, 152)
+                    n += 1
+    assert n > 300000, n
+
+
+@pytest.mark.parametrize("sms", [1, 8, 132, 148])
+def test_other_sm_counts(sms):
+    for H, R, T in itertools.product(range(256, 16385, 1280), (1, 2, 8, 16), TS):
+        for residual in (True, False):
+            _check_plan(frn.plan_launch(T, H, R, 0, residual, sms), T, H, R, 0, residual, sms)
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 8, 12, 16])
+def test_forced_cluster_sizes(ctas):
+    frn.set_kernel(frn.KERNEL_ROWS)
+    frn.set_ctas_per_row(ctas)
+    try:
+        for H, R, T in itertools.product(range(8, 16385, 136), (1, 2, 8, 16), (1, 64, 4096)):
+            pl = frn.plan_launch(T, H, R, 0, True, 152)
+            ntiles = -(-(H // 8) // 32)
+            assert pl["kernel"] == frn.KERNEL_ROWS
+            C, tpc = pl["ctas_per_row"], pl["tiles_per_cta"]
+            assert C * tpc >= ntiles and (C - 1) * tpc < ntiles and 1 <= C <= 16
+            assert pl["threads"] <= (1024 if C == 1 else 512)
+    finally:
+        frn.set_ctas_per_row(0)
+        frn.set_kernel(frn.KERNEL_AUTO)
+
+
+def test_forced_stream_groups():
+    frn.set_kernel(frn.KERNEL_STREAM)
+    try:
+        for groups in (1, 2, 3, 4):
+            frn.set_stream_groups(groups)
+            for H, R in itertools.product(range(8, 16385, 264), (1, 2, 8, 16)):
+                pl = frn.plan_launch(4096, H, R, 0, True, 152)
+                _check_plan(pl, 4096, H, R, 0, True, 152, auto=False)
+                assert pl["groups"] <= groups
+    finally:
+        frn.set_stream_groups(0)
+        frn.set_kernel(frn.KERNEL_AUTO)
+
+
+def test_plan_rejects_bad_sizes():
+    for args in ((0, 256, 2), (4, 100, 2), (4, 256, 0), (4, 256, 17), (4, 16392, 2)):
+        with pytest.raises(frn.FrnError):
+            frn.plan_launch(*args)
