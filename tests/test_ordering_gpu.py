@@ -52,6 +52,36 @@ def test_same_stream_slow_producer(pdl):
     assert_y_close(host_bits(y), ry)
 
 
+@pytest.mark.parametrize("shape", [(4, 16, 4096), (8, 16, 7168), (8, 64, 7168), (2, 700, 256)],
+                         ids=["single_cta", "cluster", "wide", "packed"])
+def test_slow_producer_with_l2_prefetch_forced_on(shape):
+    """The kernels prefetch their rows into L2 before the dependency wait.  With
+    the prefetch forced on for every row-kernel shape and a slow producer that
+    overwrites the partials (zeros before) only after ~10 ms, the prefetched
+    lines hold the old zeros, yet every value the kernel reads after the wait is
+    the producer's: L2 is where the producer's writes land."""
+    R_, T_, H_ = shape
+    inp = syn.make_inputs(R_, T_, H_, seed=52, partial_std=0.5)
+    src = dev_bf16(inp.partials)
+    buf = torch.zeros_like(src)
+    res, gamma = dev_bf16(inp.residual), dev_bf16(inp.gamma)
+    frn.set_l2_prefetch(2)
+    frn.set_kernel(frn.KERNEL_ROWS)
+    try:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(SLEEP_CYCLES)
+            buf.copy_(src)                   # the producer
+            y, ro = frn.fused_reduce_rmsnorm(buf, res, gamma, inp.eps)
+        s.synchronize()
+    finally:
+        frn.set_kernel(frn.KERNEL_AUTO)
+        frn.set_l2_prefetch(0)
+    rro, ry = _ref(inp)
+    assert_residual_exact(host_bits(ro), rro)
+    assert_y_close(host_bits(y), ry)
+
+
 def test_two_streams_event(pdl):
     inp = syn.make_inputs(R, T, H, seed=51)
     src = dev_bf16(inp.partials)
