@@ -361,23 +361,33 @@ __device__ __forceinline__ void mul2_bf16(float& p0, float& p1, uint32_t xw, uin
 // otherwise both are widened first and multiplied in fp32 (fewer live
 // registers in register-capped kernels).  The two give the same bits.
 template <bool MIXED = true>
-__device__ __forceinline__ uint4 rms_y(const uint4 xb, float rstd, const uint4 g) {
-    float yv[8];
+__device__ __forceinline__ void xgamma8(const uint4 xb, const uint4 g, float (&xg)[8]) {
     if constexpr (MIXED) {
-        mul2_bf16(yv[0], yv[1], xb.x, g.x);
-        mul2_bf16(yv[2], yv[3], xb.y, g.y);
-        mul2_bf16(yv[4], yv[5], xb.z, g.z);
-        mul2_bf16(yv[6], yv[7], xb.w, g.w);
+        mul2_bf16(xg[0], xg[1], xb.x, g.x);
+        mul2_bf16(xg[2], xg[3], xb.y, g.y);
+        mul2_bf16(xg[4], xg[5], xb.z, g.z);
+        mul2_bf16(xg[6], xg[7], xb.w, g.w);
     } else {
         float gf[8];
-        unpack8(xb, yv);
+        unpack8(xb, xg);
         unpack8(g, gf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(yv[i], gf[i]);
+        for (int i = 0; i < 8; ++i) xg[i] = __fmul_rn(xg[i], gf[i]);
     }
+}
+
+// y from the x * gamma products (xgamma8) and rstd.
+__device__ __forceinline__ uint4 y_from_xgamma(float (&xg)[8], float rstd) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(yv[i], rstd);
-    return pack8(yv);
+    for (int i = 0; i < 8; ++i) xg[i] = __fmul_rn(xg[i], rstd);
+    return pack8(xg);
+}
+
+template <bool MIXED = true>
+__device__ __forceinline__ uint4 rms_y(const uint4 xb, float rstd, const uint4 g) {
+    float xg[8];
+    xgamma8<MIXED>(xb, g, xg);
+    return y_from_xgamma(xg, rstd);
 }
 
 // Per-group dynamic e4m3 of one bf16 y vector.  All 32 lanes must call it (the

@@ -135,8 +135,18 @@ frn_row_kernel(const __grid_constant__ Params p) {
 
     const float s = tile_sumsq(ro);
 
-    // Every global store of this thread comes after the cluster synchronisation
-    // below, so that no barrier operation waits for outstanding stores.
+    // x * gamma needs no rstd: the single-CTA shapes form it before the row
+    // barrier, and store residual_out there too, so that this runs while the
+    // other warps catch up -- except with a quant output in the 512-thread
+    // shape (the early store measured slower at the FP8 decode workload) and
+    // the packed 256-thread shape (both, tight on registers).  In a cluster,
+    // every global store of this thread comes after the cluster
+    // synchronisation, so that no barrier operation waits for outstanding
+    // stores.
+    constexpr bool kQuantOut = mode_fp8(MODE) || mode_mx(MODE);
+    constexpr bool kEarlyXg = !CLUSTER && !(MAXT == kPackedThreads && kQuantOut);
+    constexpr bool kEarlyStore = kEarlyXg && !(MAXT == kMaxThreads && kQuantOut);
+    float xg[8];
     float lo, hi;   // tile slots `lane` and `lane + 32` of the row
     if constexpr (CLUSTER) {
         cluster_wait_acquire();   // every CTA of the cluster has armed its row barrier
@@ -149,6 +159,10 @@ frn_row_kernel(const __grid_constant__ Params p) {
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
         hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     } else {
+        if constexpr (kEarlyStore) {
+            if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
+        }
+        if constexpr (kEarlyXg) xgamma8(ro, g, xg);
         // this CTA's rows are consecutive groups of ntiles warps
         if (lane == 0) tile_sum[warp] = s;
         __syncthreads();
@@ -179,8 +193,11 @@ frn_row_kernel(const __grid_constant__ Params p) {
         __syncwarp();
         cluster_arrive_relaxed_after(rstd);
     }
-    if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
-    const uint4 yb = rms_y(ro, rstd, g);
+    if constexpr (!kEarlyStore) {
+        if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
+    }
+    if constexpr (!kEarlyXg) xgamma8(ro, g, xg);
+    const uint4 yb = y_from_xgamma(xg, rstd);
     if constexpr (mode_writes_y(MODE)) {
         if (valid) p.y[off] = yb;
     }
