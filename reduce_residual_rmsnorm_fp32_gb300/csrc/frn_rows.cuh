@@ -139,13 +139,13 @@ frn_row_kernel(const __grid_constant__ Params p) {
     // barrier, and store residual_out there too, so that this runs while the
     // other warps catch up -- except with a quant output in the 512-thread
     // shape (the early store measured slower at the FP8 decode workload) and
-    // the packed 256-thread shape (both, tight on registers).  In a cluster,
-    // every global store of this thread comes after the cluster
-    // synchronisation, so that no barrier operation waits for outstanding
-    // stores.
+    // the packed 256-thread shape (both, tight on registers).  A cluster forms
+    // it while the tile sums travel; every global store of its threads comes
+    // after the cluster synchronisation, so that no barrier operation waits
+    // for outstanding stores.
     constexpr bool kQuantOut = mode_fp8(MODE) || mode_mx(MODE);
-    constexpr bool kEarlyXg = !CLUSTER && !(MAXT == kPackedThreads && kQuantOut);
-    constexpr bool kEarlyStore = kEarlyXg && !(MAXT == kMaxThreads && kQuantOut);
+    constexpr bool kEarlyXg = CLUSTER || !(MAXT == kPackedThreads && kQuantOut);
+    constexpr bool kEarlyStore = !CLUSTER && kEarlyXg && !(MAXT == kMaxThreads && kQuantOut);
     float xg[8];
     float lo, hi;   // tile slots `lane` and `lane + 32` of the row
     if constexpr (CLUSTER) {
@@ -154,6 +154,7 @@ frn_row_kernel(const __grid_constant__ Params p) {
         if (tile < p.ntiles && lane < p.ctas_per_row && !(p.inject_stall && tile == 0))
             st_async_f32(cluster_addr(&tile_sum[tile], static_cast<uint32_t>(lane)), s,
                          cluster_addr(&row_bar, static_cast<uint32_t>(lane)));
+        xgamma8(ro, g, xg);   // while the other CTAs' sums travel
         if (!mbar_wait_bounded(smem_addr(&row_bar), 0u, p.wait_limit_ns) && lane == 0 && p.error_word)
             atomicOr(p.error_word, kErrWaitTimeout);
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
