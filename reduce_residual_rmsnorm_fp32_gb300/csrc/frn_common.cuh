@@ -390,19 +390,45 @@ __device__ __forceinline__ uint4 rms_y(const uint4 xb, float rstd, const uint4 g
     return y_from_xgamma(xg, rstd);
 }
 
-// Per-group dynamic e4m3 of one bf16 y vector.  All 32 lanes must call it (the
-// group absmax is a half-warp shuffle).  s = absmax / 448; q = e4m3(y / s),
-// q = 0 when s == 0.
-__device__ __forceinline__ void quant8(const uint4 yb, uint2& qq, float& sc) {
-    float yq[8];
-    unpack8(yb, yq);
+// max |element| of one bf16 vector, as fp32 (exact).
+__device__ __forceinline__ float vec_absmax(const uint4 yb) {
     uint32_t mp = absmax_bf16x2(0u, yb.x);
     mp = absmax_bf16x2(mp, yb.y);
     mp = absmax_bf16x2(mp, yb.z);
     mp = absmax_bf16x2(mp, yb.w);
-    float amax = fmaxf(__uint_as_float(mp << 16), __uint_as_float(mp & 0xFFFF0000u));
+    return fmaxf(__uint_as_float(mp << 16), __uint_as_float(mp & 0xFFFF0000u));
+}
+
+// max over an aligned group of `lanes` lanes (16: a quant group, 4: an MX block).
+template <int LANES>
+__device__ __forceinline__ float group_max(float v) {
 #pragma unroll
-    for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    for (int m = LANES / 2; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+    return v;
+}
+
+// The group's absmax of y from x * gamma, before rstd is known: every y is
+// bf16(fl32(x*gamma * rstd)) with rstd > 0, and both roundings are monotonic
+// and odd, so max |y| = bf16(fl32(max |x*gamma| * rstd)) -- the same value as
+// the max over the rounded y.
+template <int LANES>
+__device__ __forceinline__ float xgamma_group_absmax(const float (&xg)[8]) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(xg[i]));
+    return group_max<LANES>(m);
+}
+
+__device__ __forceinline__ float y_absmax_from_xgamma(float amax_xg, float rstd) {
+    return __uint_as_float(pack_bf16x2(__fmul_rn(amax_xg, rstd), 0.0f) << 16);
+}
+
+// Per-group dynamic e4m3 of one bf16 y vector, given the group's absmax of y
+// (fp32; a quant group of 128 elements is an aligned half-warp).
+// s = absmax / 448; q = e4m3(y / s), q = 0 when s == 0.
+__device__ __forceinline__ void quant8_amax(const uint4 yb, float amax, uint2& qq, float& sc) {
+    float yq[8];
+    unpack8(yb, yq);
     if (amax >= 0x1p-60f) {
         // absmax / 448, correctly rounded, without a divide: RN(absmax * RN(1/448))
         // and one FMA correction (Markstein's theorem); checked exhaustively for
@@ -442,6 +468,11 @@ __device__ __forceinline__ void quant8(const uint4 yb, uint2& qq, float& sc) {
     }
 }
 
+// Per-group dynamic e4m3 of one bf16 y vector; all 32 lanes must call it.
+__device__ __forceinline__ void quant8(const uint4 yb, uint2& qq, float& sc) {
+    quant8_amax(yb, group_max<16>(vec_absmax(yb)), qq, sc);
+}
+
 // OCP Microscaling (MX v1.0) FP4: E2M1, round to nearest even, saturating to
 // +-6; the low nibble of the result holds the second source operand.
 __device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
@@ -453,18 +484,11 @@ __device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
     return r;
 }
 
-// MXFP4 of one bf16 y vector: a block of 32 elements is an aligned group of 4
-// lanes, and all 32 lanes must call this.  shared_exp = floor(log2(absmax)) - 2
+// MXFP4 of one bf16 y vector given its block's absmax of y (fp32; a block of
+// 32 elements is an aligned group of 4 lanes).  shared_exp = floor(log2(absmax)) - 2
 // (2 = emax of E2M1), clamped to [-127, 127]; elements y * 2^-shared_exp (exact)
 // rounded to E2M1.  An all-zero block gives scale code 0 and zero elements.
-__device__ __forceinline__ void mxfp4_8(const uint4 yb, uint32_t& packed, uint32_t& code) {
-    uint32_t mp = absmax_bf16x2(0u, yb.x);
-    mp = absmax_bf16x2(mp, yb.y);
-    mp = absmax_bf16x2(mp, yb.z);
-    mp = absmax_bf16x2(mp, yb.w);
-    float amax = fmaxf(__uint_as_float(mp << 16), __uint_as_float(mp & 0xFFFF0000u));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+__device__ __forceinline__ void mxfp4_8_amax(const uint4 yb, float amax, uint32_t& packed, uint32_t& code) {
     packed = 0u;
     code = 0u;
     if (amax > 0.0f) {
@@ -491,6 +515,11 @@ __device__ __forceinline__ void mxfp4_8(const uint4 yb, uint32_t& packed, uint32
         packed = pack_e2m1x2(v[0], v[1]) | (pack_e2m1x2(v[2], v[3]) << 8) | (pack_e2m1x2(v[4], v[5]) << 16) |
                  (pack_e2m1x2(v[6], v[7]) << 24);
     }
+}
+
+// MXFP4 of one bf16 y vector; all 32 lanes must call it (a block is 4 lanes).
+__device__ __forceinline__ void mxfp4_8(const uint4 yb, uint32_t& packed, uint32_t& code) {
+    mxfp4_8_amax(yb, group_max<4>(vec_absmax(yb)), packed, code);
 }
 
 }  // namespace frn
