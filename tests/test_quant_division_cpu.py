@@ -62,3 +62,25 @@ def test_fma_corrected_scale_is_correctly_rounded():
             q0 = rn32(aa * c)
             rem = rn32(aa - 448 * q0)
             assert rn32(q0 + rem * c) == rn32(aa / 448), (m, shift)
+
+
+def test_group_absmax_from_x_gamma():
+    """The row kernel takes an FP8 group's absmax of y from x*gamma before rstd
+    is known: y = bf16(fl32(x*gamma * rstd)) with rstd > 0, so
+    max |y| == bf16(fl32(max |x*gamma| * rstd)).  Checked on random groups,
+    including ties, zeros, subnormal-scale and overflow-scale values."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(17)
+    for trial in range(400):
+        scale = float(2.0 ** rng.integers(-140, 120))
+        xg = (rng.standard_normal(128) * scale).astype(np.float32)
+        if trial % 7 == 0:
+            xg[rng.integers(0, 128, 5)] = 0.0
+        if trial % 11 == 0:
+            xg[3] = -xg[9]                                  # a tie in magnitude
+        rstd = np.float32(2.0 ** rng.uniform(-20, 20))
+        y = torch.from_numpy(xg * rstd).to(torch.bfloat16).float().numpy()
+        lhs = np.max(np.abs(y))
+        rhs = torch.from_numpy(np.array([np.max(np.abs(xg)) * rstd], dtype=np.float32)).to(torch.bfloat16).float()
+        assert lhs == rhs.item() or (np.isinf(lhs) and np.isinf(rhs.item())), (trial, lhs, rhs)
