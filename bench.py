@@ -12,7 +12,14 @@ input set (four launches each), as a decode engine's graph holds the epilogues
 of all its layers.
 
 Besides the JSON contract keys, the line carries:
-  decode_us_per_call  per T: graph replay and raw (Python-launched) calls
+  decode_us_per_call  per T: graph replay and raw (Python-launched) calls;
+                      the floor of the same graph shape (empty kernel, a
+                      read-only and a read+write kernel of the same bytes);
+                      the call right after a producer kernel that writes its
+                      partials (L2 prefetch as chosen, and off), with the
+                      floor kernels measured the same way
+  host_us_per_call    host time per back-to-back call at T=8: the C entry
+                      point through ctypes, the Python binding, a bare launch
   large_T             the >= 1024-token workloads: the message sweep at
                       16/32/64 MB per partial and the 8192-token prefill chunk
                       with per-group FP8 quant (both output variants), without
@@ -263,8 +270,22 @@ def time_graph(g, calls_per_replay: int, min_seconds: float = 0.05, max_reps: in
 
 
 def measure_decode_per_T(frn):
-    """µs per call at each decode T: graph replay over enough rotating sets to
-    defeat L2, and raw calls launched one by one from Python."""
+    """µs per call at each decode T, each next to its floor.
+
+    * graph_us: the fused call in a CUDA graph over enough rotating input sets
+      to defeat L2, every call independent of the one before it (the previous
+      call's tail overlaps this call's start: programmatic dependent launch,
+      and the row kernel's L2 prefetch before its dependency wait);
+    * floor_us: the library's reference kernels in the same graph shape -- an
+      empty kernel on the fused call's grid, a kernel that only loads the same
+      input bytes, and one that loads them and stores the same output bytes
+      (frn_floor_launch);
+    * after_producer_us: the pages' setting, where the kernel right before the
+      call writes the partials (here a copy into them): a graph of
+      (producer, fused call) pairs minus a graph of the producers alone; with
+      the L2 prefetch as the library decides it and with it off, and the
+      floor kernels measured the same way;
+    * raw_launch_us: calls launched one by one from Python (host-bound)."""
     out = {}
     gamma = syn.make_inputs_device(1, 1, H, seed=7)[2]
     for T in DECODE_T:
@@ -275,25 +296,112 @@ def measure_decode_per_T(frn):
             p, r, _ = syn.make_inputs_device(R_DEC, T, H, seed=1000 + k, partial_std=0.5)
             sets.append((p, r, torch.empty((T, H), dtype=torch.bfloat16, device="cuda"),
                          torch.empty((T, H), dtype=torch.bfloat16, device="cuda")))
+        _, _, threads, grid = frn.query_launch(T, H, R_DEC)
 
-        def body():
-            for p, r, ro, y in sets:
-                frn.fused_reduce_rmsnorm(p, r, gamma, EPS, residual_out=ro, y=y)
-        g = capture(body)
-        t_graph = time_graph(g, n, min_seconds=0.1)
+        def fused(st):
+            p, r, ro, y = st
+            frn.fused_reduce_rmsnorm(p, r, gamma, EPS, residual_out=ro, y=y)
+
+        def empty(st):
+            frn.floor_launch(frn.FLOOR_EMPTY, threads=threads, grid=grid)
+
+        def read(st):
+            p, r, ro, y = st
+            frn.floor_launch(frn.FLOOR_READ, [p[i] for i in range(R_DEC)] + [r])
+
+        def copy(st):
+            p, r, ro, y = st
+            frn.floor_launch(frn.FLOOR_COPY, [p[i] for i in range(R_DEC)] + [r], ro, y)
+
+        def chain(fn):
+            g = capture(lambda: [fn(st) for st in sets])
+            t = time_graph(g, n, min_seconds=0.1)
+            del g
+            return t
+
+        t_graph = chain(fused)
+        floor = {"empty_us": chain(empty), "read_us": chain(read), "copy_us": chain(copy)}
+        # the producer-then-fuse setting
+        src = [torch.randn((R_DEC, T, H), device="cuda").to(torch.bfloat16) for _ in range(2)]
+
+        def with_producer(fn):
+            def body():
+                for k, st in enumerate(sets):
+                    st[0].copy_(src[k % 2])
+                    if fn is not None:
+                        fn(st)
+            g = capture(body)
+            t = time_graph(g, n, min_seconds=0.1)
+            del g
+            return t
+        t_prod = with_producer(None)
+        after = {"producer_us": t_prod, "fused_us": with_producer(fused) - t_prod}
+        frn.set_l2_prefetch(1)
+        try:
+            after["fused_no_prefetch_us"] = with_producer(fused) - t_prod
+        finally:
+            frn.set_l2_prefetch(0)
+        after["empty_us"] = with_producer(empty) - t_prod
+        after["copy_us"] = with_producer(copy) - t_prod
         # raw launches
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         reps = max(1, 2000 // n)
         e0.record()
         for _ in range(reps):
-            body()
+            for st in sets:
+                fused(st)
         e1.record()
         torch.cuda.synchronize()
         t_raw = e0.elapsed_time(e1) / 1e3 / (reps * n)
-        out[str(T)] = {"graph_us": round(t_graph * 1e6, 3), "raw_launch_us": round(t_raw * 1e6, 3),
-                       "bytes": fp, "graph_GBps": round(fp / t_graph / 1e9, 1), "input_sets": n}
-        del sets, g
+        us = lambda t: round(t * 1e6, 3)  # noqa: E731
+        out[str(T)] = {
+            "graph_us": us(t_graph), "raw_launch_us": us(t_raw), "bytes": fp,
+            "graph_GBps": round(fp / t_graph / 1e9, 1), "input_sets": n,
+            "floor_us": {k: us(v) for k, v in floor.items()},
+            "of_copy_floor": round(t_graph / floor["copy_us"], 3),
+            "after_producer_us": us(after["fused_us"]),
+            "after_producer_no_prefetch_us": us(after["fused_no_prefetch_us"]),
+            "floor_after_producer_us": {"empty_us": us(after["empty_us"]), "copy_us": us(after["copy_us"]),
+                                        "producer_us": us(t_prod)},
+            "after_producer_of_copy_floor": round(after["fused_us"] / after["copy_us"], 3),
+            "launch": {"threads": threads, "ctas": grid},
+        }
+        del sets, src
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_host_cost(frn, calls: int = 20000):
+    """Host time per call at T = 8 (R = 8, H = 7168), back to back, no graph:
+    the C entry point called through a prebuilt ctypes argument list, the
+    Python binding, and a bare launch of the empty reference kernel through the
+    same ctypes path (ctypes overhead plus one cudaLaunchKernelEx)."""
+    import ctypes
+    T = 8
+    p, r, g = syn.make_inputs_device(R_DEC, T, H, seed=11, partial_std=0.5)
+    ro = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(ro)
+    lib = frn.library()
+    arr = (ctypes.c_void_p * R_DEC)(*[p[i].data_ptr() for i in range(R_DEC)])
+    s = torch.cuda.current_stream().cuda_stream
+    args = (arr, R_DEC, r.data_ptr(), g.data_ptr(), ro.data_ptr(), y.data_ptr(), T, H, ctypes.c_float(EPS), s)
+    empty_args = (0, None, 0, None, None, 0, 32, 1, 1, s)
+    out = {}
+    for name, fn in (("c_abi_via_ctypes_us", lambda: lib.fused_reduce_rmsnorm(*args)),
+                     ("binding_us", lambda: frn.fused_reduce_rmsnorm(p, r, g, EPS, residual_out=ro, y=y)),
+                     ("bare_launch_via_ctypes_us", lambda: lib.frn_floor_launch(*empty_args))):
+        for _ in range(200):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        out[name] = round((t1 - t0) / calls * 1e6, 3)
+    out["library_over_bare_launch_us"] = round(out["c_abi_via_ctypes_us"] - out["bare_launch_via_ctypes_us"], 3)
+    out["calls"] = calls
     return out
 
 
@@ -644,13 +752,23 @@ def main():
         for st in sets:
             st.step(frn)
     chain = capture(all_sets)
-    graphs = [capture(lambda s=s: s.step(frn)) for s in sets]
+    tails = {}
+
+    def tail(k):
+        """A graph of the first k steps of a pass, captured ahead of the timed region."""
+        if k not in tails:
+            tails[k] = capture(lambda: [sets[i].step(frn) for i in range(k)])
+        return tails[k]
+    for k in {args.steps % nsets, args.warmup % nsets} - {0}:
+        tail(k)
 
     def run_steps(n):
+        """n steps: whole passes as replays of the chain graph, the rest as one
+        graph of exactly that many steps, so every step runs the same way."""
         for _ in range(n // nsets):
             chain.replay()
-        for k in range(n % nsets):
-            graphs[k].replay()
+        if n % nsets:
+            tail(n % nsets).replay()
 
     # clocks are sampled from here to the end of the timed region: a ~0.5 s
     # stretch of the same steps first (part of the warm-up), then the timed steps
@@ -674,7 +792,7 @@ def main():
     elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     bytes_per_step = step_bytes()
     value = world * bytes_per_step * args.steps / elapsed / 1e9
-    del chain, graphs, sets
+    del chain, tails, sets
     torch.cuda.empty_cache()
 
     extras = {}
@@ -682,6 +800,7 @@ def main():
     if not args.no_extras:
         dec = measure_decode_per_T(frn)
         extras["decode_us_per_call"] = dec
+        extras["host_us_per_call"] = measure_host_cost(frn)
         t64 = dec["64"]["graph_us"] / 1e6
         b64 = dec["64"]["bytes"]
         ach = b64 / t64 / 1e9
@@ -722,7 +841,8 @@ def main():
         "data": "synthetic (seeded torch.randn on device, bf16 inputs)",
         "config": {"workload": WORKLOAD, "R": R_DEC, "H": H, "T": list(DECODE_T),
                    "launch": f"CUDA graph replay, one graph per pass over the {nsets} input sets "
-                             f"({nsets} steps, {nsets * len(DECODE_T)} kernels)",
+                             f"({nsets} steps, {nsets * len(DECODE_T)} kernels), the remaining "
+                             f"steps % {nsets} as one graph of exactly that many steps",
                    "l2": f"{nsets} rotating input sets, {nsets * per_set / 1e6:.0f} MB > 2x L2 "
                          f"({l2_bytes() / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
         "frac_of_hbm": round(value / world / hbm, 4), "hbm_peak_gbs": hbm, "hbm_peak_kind": peak_kind,

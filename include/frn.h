@@ -71,6 +71,11 @@
  *    Work queued earlier on the stream (e.g. the producers of the partials)
  *    is complete before the kernel reads anything; calls on different streams
  *    that share buffers must be ordered by the caller (events).
+ *  - On its first use on a device the library looks up and keeps, for the
+ *    life of the process, that device's SM count and the device addresses of
+ *    its own status word and static workspace.  cudaDeviceReset (or any other
+ *    teardown of the device's primary context) makes the kept addresses stale:
+ *    do not call the library on a device after resetting it.
  */
 #ifndef FRN_H_
 #define FRN_H_
@@ -239,6 +244,29 @@ frn_status frn_unfused_reduce_rmsnorm_noalloc(const void* const* partials, int R
                                               int64_t T, int H, float eps, int group_size,
                                               int stages, frn_stream_t stream);
 
+/*
+ * Measurement reference kernels (no entry point of the op uses them).  A
+ * decode-sized call is mostly fixed cost -- launch and hand-off from the
+ * previous kernel, one DRAM round trip, the drain of its stores -- so its
+ * speed is judged against kernels that have that cost and nothing else,
+ * launched the same way (pdl != 0: programmatic dependent launch, with the
+ * grid-dependency wait before the first global access):
+ *   kind 0  empty kernel: grid_ctas CTAs of `threads` threads (srcs, dst0,
+ *           dst1 and nbytes unused);
+ *   kind 1  read: each thread loads one 16-byte vector of each of the n_src
+ *           (1..17) device buffers of nbytes bytes (a multiple of 16), through
+ *           the op's load path, and stores nothing;
+ *   kind 2  copy: the same loads, then stores of nbytes bytes into each of
+ *           dst0 and dst1 -- the traffic of a call without quant (R partials
+ *           and the residual in; residual_out and y out) without its arithmetic.
+ * Kinds 1 and 2 launch ceil(nbytes / 16 / threads) CTAs (grid_ctas unused).
+ * threads: a multiple of 32 in 32..1024.  All pointers 16-byte aligned.
+ * Returns FRN_ERR_INVALID_ARG / FRN_ERR_MISALIGNED without launching on bad
+ * arguments, FRN_ERR_CUDA on a launch error; frn_last_error_detail is not set.
+ */
+frn_status frn_floor_launch(int kind, const void* const* srcs, int n_src, void* dst0, void* dst1,
+                            int64_t nbytes, int threads, int64_t grid_ctas, int pdl, frn_stream_t stream);
+
 /* Static text for a status code. */
 const char* frn_status_string(frn_status s);
 
@@ -325,12 +353,14 @@ frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int has_residual,
 /*
  * Report the launch a call with these sizes would use on the current device:
  * kernel (1 row, 2 stream), CTAs per row (cluster size; 1 for the stream
- * kernel and for a single wide CTA), threads per CTA, and CTAs in the grid.
- * quant: 0 no quant, 1 / 2 per-group FP8 without / with y, 3 / 4 MXFP4
- * without / with y.  Output pointers may be NULL.
+ * kernel and for a single wide CTA), threads per CTA, and CTAs in the grid --
+ * frn_plan_launch with the current device's SM count.  quant: 0 no quant,
+ * 1 / 2 per-group FP8 without / with y, 3 / 4 MXFP4 without / with y.
+ * has_residual != 0 when the call passes a residual.  T == 0 reports the
+ * shape of a one-row call with a grid of 0.  Output pointers may be NULL.
  */
-frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int* ctas_per_row,
-                            int* threads_per_cta, int64_t* grid_ctas);
+frn_status frn_query_launch(int64_t T, int H, int R, int quant, int has_residual, int* kernel,
+                            int* ctas_per_row, int* threads_per_cta, int64_t* grid_ctas);
 
 /*
  * Device-side failure detection.  Every device-side wait is bounded (default

@@ -83,7 +83,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_set_stream_groups.restype = i32
     lib.frn_plan_launch.argtypes = [i64, i32, i32, i32, i32, i32, vp]
     lib.frn_plan_launch.restype = i32
-    lib.frn_query_launch.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+    lib.frn_query_launch.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                      ctypes.POINTER(i32), ctypes.POINTER(i64)]
     lib.frn_query_launch.restype = i32
     lib.frn_device_status.argtypes = [i32]
@@ -104,6 +104,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.frn_unfused_reduce_rmsnorm_noalloc.argtypes = [ctypes.POINTER(vp), i32, vp, vp, vp, vp, vp, vp, i64, i32,
                                                        f32, i32, i32, vp]
     lib.frn_unfused_reduce_rmsnorm_noalloc.restype = i32
+    lib.frn_floor_launch.argtypes = [i32, ctypes.POINTER(vp), i32, vp, vp, i64, i32, i64, i32, vp]
+    lib.frn_floor_launch.restype = i32
     return lib
 
 
@@ -173,12 +175,13 @@ def plan_launch(T: int, H: int, R: int, quant: int = 0, residual: bool = True, n
     return {name: getattr(out, name) for name, _ in _LaunchPlan._fields_}
 
 
-def query_launch(T: int, H: int, R: int, quant: int = 0) -> tuple[int, int, int, int]:
+def query_launch(T: int, H: int, R: int, quant: int = 0, residual: bool = True) -> tuple[int, int, int, int]:
     """(kernel, ctas_per_row, threads_per_cta, grid_ctas) a call would use on the current device.
-    quant: 0 none, 1 / 2 FP8 without / with y, 3 / 4 MXFP4 without / with y."""
+    quant: 0 none, 1 / 2 FP8 without / with y, 3 / 4 MXFP4 without / with y; residual: whether the
+    call passes one."""
     k, c, t, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
-    _check(library().frn_query_launch(int(T), int(H), int(R), int(quant), ctypes.byref(k), ctypes.byref(c),
-                                      ctypes.byref(t), ctypes.byref(g)))
+    _check(library().frn_query_launch(int(T), int(H), int(R), int(quant), 1 if residual else 0, ctypes.byref(k),
+                                      ctypes.byref(c), ctypes.byref(t), ctypes.byref(g)))
     return k.value, c.value, t.value, g.value
 
 
@@ -319,6 +322,26 @@ def unfused_workspace_bytes(T: int, H: int, stages: int, quant: bool, emit_y: bo
                                                      int(bool(emit_y))))
 
 
+def _check_unfused_outputs(T, H, dev, quant, group_size, residual_out, y, q, scales) -> None:
+    """The unfused paths' outputs: the C side sees only pointers, so every
+    tensor's device, dtype, shape and layout is checked here, before anything is
+    launched."""
+    _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev, out=True)
+    if y is not None:
+        _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
+    if quant:
+        if group_size < 1 or H % group_size:
+            raise ValueError(f"group_size={group_size} must divide H={H}")
+        if q is None or scales is None:
+            raise ValueError("quant needs both q and scales")
+        if q.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError("q must be float8_e4m3fn or uint8")
+        _check_tensor(q, "q", q.dtype, (T, H), dev, out=True)
+        _check_tensor(scales, "scales", torch.float32, (T, H // group_size), dev, out=True)
+    elif y is None:
+        raise ValueError("without quant, y is the output and must be given")
+
+
 def unfused_reduce_rmsnorm(partials, residual: torch.Tensor | None, gamma: torch.Tensor, eps: float = 1e-6, *,
                            stages: int = 2, quant: bool = False, emit_bf16: bool = True,
                            group_size: int = QUANT_GROUP, workspace: torch.Tensor | None = None,
@@ -349,6 +372,11 @@ def unfused_reduce_rmsnorm(partials, residual: torch.Tensor | None, gamma: torch
             q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=dev)
         if scales is None:
             scales = torch.empty((T, H // group_size), dtype=torch.float32, device=dev)
+    _check_unfused_outputs(T, H, dev, quant, group_size, residual_out, y, q, scales)
+    if workspace.device != dev:
+        raise ValueError(f"workspace must be on {dev} (got {workspace.device})")
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
     arr = (ctypes.c_void_p * R)(*ptrs)
     with _on(dev):
         st = library().frn_unfused_reduce_rmsnorm(
@@ -374,12 +402,44 @@ def unfused_reduce_rmsnorm_noalloc(partials, residual: torch.Tensor | None, gamm
     any stream capture, and calls that can overlap on the GPU race on the shared
     scratch."""
     ptrs, R, T, H, dev = _partials(partials)
+    if residual is not None:
+        _check_tensor(residual, "residual", torch.bfloat16, (T, H), dev)
+    _check_tensor(gamma, "gamma", torch.bfloat16, (H,), dev)
+    if (q is None) != (scales is None):
+        raise ValueError("pass both q and scales (quant) or neither")
+    _check_unfused_outputs(T, H, dev, q is not None, group_size, residual_out, y, q, scales)
     arr = (ctypes.c_void_p * R)(*ptrs)
     with _on(dev):
         st = library().frn_unfused_reduce_rmsnorm_noalloc(
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales), T, H,
             float(eps), int(group_size), int(stages), _stream(stream, dev))
     _check(st)
+
+
+FLOOR_EMPTY, FLOOR_READ, FLOOR_COPY = 0, 1, 2
+
+
+def floor_launch(kind: int, sources: Sequence[torch.Tensor] = (), dst0: torch.Tensor | None = None,
+                 dst1: torch.Tensor | None = None, threads: int = 128, grid: int = 1, pdl: bool = True,
+                 stream=None) -> None:
+    """Launch one of the measurement reference kernels (frn_floor_launch in frn.h):
+    FLOOR_EMPTY (``grid`` CTAs of ``threads``), FLOOR_READ (one 16-byte load per
+    thread of every source) or FLOOR_COPY (the same loads, stores into dst0 and
+    dst1).  Sources and destinations are contiguous CUDA tensors of one size."""
+    srcs = list(sources)
+    nbytes = 0
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if srcs:
+        nbytes = srcs[0].numel() * srcs[0].element_size()
+        dev = srcs[0].device
+        for t in srcs + [t for t in (dst0, dst1) if t is not None]:
+            if t.device != dev or not t.is_contiguous() or t.numel() * t.element_size() != nbytes:
+                raise ValueError("floor_launch buffers must be contiguous, on one device, of one size")
+    arr = (ctypes.c_void_p * max(1, len(srcs)))(*[t.data_ptr() for t in srcs])
+    st = library().frn_floor_launch(int(kind), arr if srcs else None, len(srcs), _ptr(dst0), _ptr(dst1), nbytes,
+                                    int(threads), int(grid), 1 if pdl else 0, _stream(stream, dev))
+    if st != FRN_OK:
+        raise FrnError(st, "frn_floor_launch")
 
 
 def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None, gamma: torch.Tensor, eps: float = 1e-6, *,

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfrn.so")
 SOURCES = ["frn_api.cu", "frn_launch_norm.cu", "frn_launch_quant_a.cu", "frn_launch_quant_b.cu",
-           "frn_launch_unfused.cu", "frn_launch_mx_a.cu", "frn_launch_mx_b.cu"]
+           "frn_launch_unfused.cu", "frn_launch_mx_a.cu", "frn_launch_mx_b.cu", "frn_floor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-Xcompiler", "-Wall"]

@@ -740,25 +740,22 @@ FRN_EXPORT frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int ha
     return ok();
 }
 
-FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int* kernel, int* ctas_per_row,
-                                       int* threads_per_cta, int64_t* grid_ctas) {
-    if (R < 1 || T < 0 || H < 8 || H % 8 != 0 || H > FRN_MAX_HIDDEN || quant < 0 || quant > 4)
+FRN_EXPORT frn_status frn_query_launch(int64_t T, int H, int R, int quant, int has_residual, int* kernel,
+                                       int* ctas_per_row, int* threads_per_cta, int64_t* grid_ctas) {
+    if (R < 1 || R > FRN_MAX_PARTIALS || T < 0 || H < 8 || H % 8 != 0 || H > FRN_MAX_HIDDEN || quant < 0 ||
+        quant > 4)
         return fail(FRN_ERR_INVALID_ARG, "bad sizes");
     int sms = 0;
     frn_status st = sm_count(&sms);
     if (st != FRN_OK) return st;
-    const int kind = choose_kind(T, H, R, quant, sms);
-    if (kernel) *kernel = kind;
-    if (kind == kStream) {
-        const frn::StreamPlan plan = choose_stream(T, H, R + 1, sms);
-        if (ctas_per_row) *ctas_per_row = 1;
-        if (threads_per_cta) *threads_per_cta = (plan.groups * plan.consumer_warps + 1) * 32;
-        if (grid_ctas) *grid_ctas = plan.grid;
-    } else {
-        const frn::RowPlan plan = choose_rows(T, H, R, sms);
-        if (ctas_per_row) *ctas_per_row = plan.ctas_per_row;
-        if (threads_per_cta) *threads_per_cta = plan.threads;
-        if (grid_ctas) *grid_ctas = plan.grid;
-    }
+    // the plan of a call with these sizes on this device's SM count (T = 0
+    // launches nothing; it reports the plan of one row)
+    frn_launch_plan plan;
+    st = frn_plan_launch(T > 0 ? T : 1, H, R, quant, has_residual, sms, &plan);
+    if (st != FRN_OK) return st;
+    if (kernel) *kernel = plan.kernel;
+    if (ctas_per_row) *ctas_per_row = plan.ctas_per_row;
+    if (threads_per_cta) *threads_per_cta = plan.threads;
+    if (grid_ctas) *grid_ctas = T > 0 ? plan.grid : 0;
     return ok();
 }

@@ -129,3 +129,16 @@ def test_binding_rejects_host_inputs():
         frn.fused_reduce_rmsnorm(p, None, g, 1e-6)
     with pytest.raises(ValueError, match="must be on"):
         frn.fused_reduce_rmsnorm_quant_per_group(p, None, g, 1e-6)
+
+
+def test_floor_launch_validates_without_launching(lib):
+    """Bad arguments to the measurement kernels are refused on the host."""
+    arr = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    assert lib.frn_floor_launch(3, arr, 2, None, None, 64, 128, 1, 1, None) == frn.FRN_ERR_INVALID_ARG
+    assert lib.frn_floor_launch(1, arr, 2, None, None, 64, 100, 1, 1, None) == frn.FRN_ERR_INVALID_ARG
+    assert lib.frn_floor_launch(1, arr, 0, None, None, 64, 128, 1, 1, None) == frn.FRN_ERR_INVALID_ARG
+    assert lib.frn_floor_launch(1, arr, 2, None, None, 40, 128, 1, 1, None) == frn.FRN_ERR_INVALID_ARG
+    assert lib.frn_floor_launch(2, arr, 2, 0x3000, None, 64, 128, 1, 1, None) == frn.FRN_ERR_INVALID_ARG
+    bad = (ctypes.c_void_p * 2)(0x1000, 0x2008)
+    assert lib.frn_floor_launch(1, bad, 2, None, None, 64, 128, 1, 1, None) == frn.FRN_ERR_MISALIGNED
+    assert lib.frn_floor_launch(0, None, 0, None, None, 0, 128, 0, 1, None) == frn.FRN_ERR_INVALID_ARG

@@ -109,3 +109,17 @@ def test_plan_rejects_bad_sizes():
     for args in ((0, 256, 2), (4, 100, 2), (4, 256, 0), (4, 256, 17), (4, 16392, 2)):
         with pytest.raises(frn.FrnError):
             frn.plan_launch(*args)
+
+
+def test_query_launch_checks_sizes_then_needs_a_device():
+    """frn_query_launch is frn_plan_launch with the current device's SM count:
+    bad sizes are refused before any device is touched, and on a host without
+    a GPU the SM-count lookup fails with FRN_ERR_CUDA."""
+    import ctypes
+    import torch
+    lib = frn.library()
+    k = ctypes.c_int()
+    for bad in ((8, 7168, 0, 0), (8, 7168, 17, 0), (-1, 7168, 8, 0), (8, 7100, 8, 0), (8, 7168, 8, 5)):
+        assert lib.frn_query_launch(*bad, 1, ctypes.byref(k), None, None, None) == frn.FRN_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert lib.frn_query_launch(8, 7168, 8, 0, 0, ctypes.byref(k), None, None, None) == frn.FRN_ERR_CUDA

@@ -5,6 +5,8 @@ Matching rule: residual_out bit-exact, y within one bf16 ulp; in every block
 whose y equals the oracle's bit for bit, the E8M0 code and all E2M1 codes are
 equal; elsewhere (a 1-ulp y flip) E2M1 codes differ by at most one step, on at
 most 0.1% of all elements."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -12,22 +14,14 @@ import torch
 import oracle
 import reduce_residual_rmsnorm_fp32_gb300 as frn
 from reduce_residual_rmsnorm_fp32_gb300 import synthetic as syn
-from frn_testlib import DevInputs, assert_residual_exact, assert_y_close, host_bits
+from frn_testlib import DevInputs, assert_mx_close, assert_residual_exact, assert_y_close, host_bits
 
 pytestmark = pytest.mark.gpu
 
-
-def _codes(q):
-    T, Hh = q.shape
-    return np.stack([q & 0xF, q >> 4], axis=-1).reshape(T, 2 * Hh)
+THREADS = max(1, os.cpu_count() or 1)   # the oracle splits rows over the host's cores
 
 
-def _ordered_e2m1(c):
-    c = c.astype(np.int32)
-    return np.where(c & 0x8, -(c & 0x7), c & 0x7)
-
-
-def check_mx(inp, what, rows=None):
+def check_mx(inp, what):
     d = DevInputs(inp)
     (qa, sa), roa = frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps)
     (y, qb, sb), rob = frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, inp.eps, emit_bf16=True)
@@ -36,22 +30,12 @@ def check_mx(inp, what, rows=None):
     assert torch.equal(qa, qb) and torch.equal(sa, sb) and torch.equal(roa, rob) and torch.equal(roa, ron)
     assert torch.equal(y, yn)
     ro, yb, q, s = host_bits(rob), host_bits(y), host_bits(qb), host_bits(sb)
-    sub = inp
-    if rows is not None:
-        sub = syn.Inputs(inp.partials[:, rows], inp.residual[rows], inp.gamma, inp.eps)
-        ro, yb, q, s = ro[rows], yb[rows], q[rows], s[rows]
-    rro, ry, rq, rs = oracle.Oracle().reduce_rmsnorm_mxfp4(sub.partials, sub.residual, sub.gamma, sub.eps, threads=8)
+    rro, ry, rq, rs = oracle.Oracle().reduce_rmsnorm_mxfp4(inp.partials, inp.residual, inp.gamma, inp.eps,
+                                                           threads=THREADS)
     assert_residual_exact(ro, rro, what)
     assert_y_close(yb, ry, what)
-    T, H = yb.shape
-    same = np.all(yb.reshape(T, H // 32, 32) == ry.reshape(T, H // 32, 32), axis=-1)
-    c, rc = _codes(q).reshape(T, H // 32, 32), _codes(rq).reshape(T, H // 32, 32)
-    assert np.array_equal(s[same], rs[same]), what
-    assert np.array_equal(c[same], rc[same]), what
-    dc = np.abs(_ordered_e2m1(c) - _ordered_e2m1(rc))
-    assert dc.max(initial=0) <= 1, what
-    assert (dc > 0).mean() <= 1e-3, what
-    return int((~same).sum())
+    assert_mx_close(None, host_bits(qa), host_bits(sa), ry, rq, rs, what + " (A)")
+    return assert_mx_close(yb, q, s, ry, rq, rs, what + " (B)")
 
 
 @pytest.fixture(params=[frn.KERNEL_ROWS, frn.KERNEL_STREAM], ids=["rows", "stream"])
@@ -68,10 +52,8 @@ def test_mxfp4_parity(R, T, H, kernel):
 
 
 def test_mxfp4_prefill_outliers():
-    inp = syn.config_prefill(seed=4)
-    rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([rng.choice(inp.T, 40, replace=False), [0, inp.T - 1]]))
-    check_mx(inp, "mx prefill", rows=rows)
+    """Every one of the 8192 rows of the prefill chunk."""
+    check_mx(syn.config_prefill(seed=4), "mx prefill")
 
 
 @pytest.mark.parametrize("scale", [2.0 ** -100, 2.0 ** -30, 2.0 ** 40])

@@ -72,3 +72,64 @@ def test_mxfp4_and_adjacent_ops_match_binding():
     y2, ro2 = torch.ops.frn.fused_add_rmsnorm(parts[0], res, g, 1e-6)
     assert torch.equal(y2, ya) and torch.equal(ro2, roa)
     assert torch.equal(torch.ops.frn.rmsnorm(parts[0], g, 1e-6), frn.rmsnorm(parts[0], g, inp.eps))
+
+
+# ----------------------------------------------------- ops vs the oracle --
+
+def _op_inputs(R, T, H, with_residual, seed):
+    from frn_testlib import dev_bf16
+    inp = syn.make_inputs(R, T, H, seed=seed, partial_std=0.5, with_residual=with_residual)
+    parts = [dev_bf16(inp.partials[r]) for r in range(R)]
+    res = dev_bf16(inp.residual) if with_residual else None
+    return inp, parts, res, dev_bf16(inp.gamma)
+
+
+def _call(fn, compiled):
+    return torch.compile(fn, fullgraph=True)() if compiled else fn()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("compiled", [False, True], ids=["eager", "compiled"])
+@pytest.mark.parametrize("with_residual", [True, False], ids=["residual", "no_residual"])
+@pytest.mark.parametrize("R,T,H", [(8, 64, 7168), (4, 32, 4096)])
+def test_ops_against_oracle(R, T, H, with_residual, compiled):
+    """Every torch.ops.frn.* output, eager and under torch.compile, element by
+    element against the oracle under the matching rules."""
+    import oracle
+    from frn_testlib import (assert_mx_close, assert_quant_close, assert_residual_exact, assert_y_close,
+                             host_bits)
+    inp, parts, res, g = _op_inputs(R, T, H, with_residual, seed=R * 100 + T)
+    orc = oracle.Oracle()
+    rro, ry, rq, rs = orc.reduce_rmsnorm_quant(inp.partials, inp.residual, inp.gamma, inp.eps, 128)
+    _, _, rq4, re8 = orc.reduce_rmsnorm_mxfp4(inp.partials, inp.residual, inp.gamma, inp.eps)
+    eps = inp.eps
+    what = f"R={R} T={T} H={H} residual={with_residual} compiled={compiled}"
+
+    y, ro = _call(lambda: torch.ops.frn.fused_reduce_rmsnorm(parts, res, g, eps), compiled)
+    assert_residual_exact(host_bits(ro), rro, what)
+    assert_y_close(host_bits(y), ry, what)
+    for emit in (False, True):
+        y, q, s, ro = _call(lambda: torch.ops.frn.fused_reduce_rmsnorm_quant_per_group(parts, res, g, eps, 128, emit),
+                            compiled)
+        assert_residual_exact(host_bits(ro), rro, what)
+        yb = host_bits(y) if emit else None
+        if emit:
+            assert_y_close(yb, ry, what)
+        else:
+            assert y.shape == (0, H)
+        assert_quant_close(yb, host_bits(q), host_bits(s), ry, rq, rs, what + f" fp8 emit={emit}")
+        y, q4, e8, ro = _call(lambda: torch.ops.frn.fused_reduce_rmsnorm_mxfp4(parts, res, g, eps, emit), compiled)
+        assert_residual_exact(host_bits(ro), rro, what)
+        if emit:
+            assert_y_close(host_bits(y), ry, what)
+        assert_mx_close(host_bits(y) if emit else None, host_bits(q4), host_bits(e8), ry, rq4, re8,
+                        what + f" mxfp4 emit={emit}")
+    # the adjacent ops: one activation plus the residual, and a plain RMSNorm
+    one = syn.Inputs(inp.partials[:1], inp.residual, inp.gamma, eps)
+    aro, ay = orc.reduce_rmsnorm(one.partials, one.residual, one.gamma, eps)
+    y, ro = _call(lambda: torch.ops.frn.fused_add_rmsnorm(parts[0], res, g, eps), compiled)
+    assert_residual_exact(host_bits(ro), aro, what + " fused_add_rmsnorm")
+    assert_y_close(host_bits(y), ay, what + " fused_add_rmsnorm")
+    _, ny = orc.reduce_rmsnorm(inp.partials[:1], None, inp.gamma, eps)
+    y = _call(lambda: torch.ops.frn.rmsnorm(parts[0], g, eps), compiled)
+    assert_y_close(host_bits(y), ny, what + " rmsnorm")

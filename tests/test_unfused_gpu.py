@@ -1,7 +1,10 @@
 """The unfused comparison paths (3 kernels: reduce -> add + RMSNorm -> quant;
 2 kernels: fused reduce + RMSNorm -> stand-alone quant, or reduce -> add +
-RMSNorm without quant) return the same bits as the fused entry points, and
-therefore match the oracle under the same rules."""
+RMSNorm without quant): each is compared with the oracle element by element,
+with and without a residual, at a decode shape and at the prefill chunk, and
+with the fused entry points bit for bit."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -40,6 +43,54 @@ def test_unfused_quant_matches_fused(R, T, H, stages, emit):
     if emit:
         assert np.array_equal(host_bits(out[0]), base[1])
     assert np.array_equal(got_q, base[2]) and np.array_equal(got_s.view(np.uint32), base[3].view(np.uint32))
+
+
+THREADS = max(1, os.cpu_count() or 1)
+_CACHE = {}
+
+
+def _workload(name, with_residual):
+    """Decode (R=8, T=64, H=7168) or prefill (R=2, T=8192, H=7168, 1% outlier
+    channels) inputs, on the host and the device, and the oracle's outputs."""
+    key = (name, with_residual)
+    if key not in _CACHE:
+        if name == "decode":
+            inp = syn.make_inputs(8, 64, 7168, seed=94, partial_std=0.5, with_residual=with_residual)
+        else:
+            inp = syn.make_inputs(2, 8192, 7168, seed=95, outlier_frac=0.01, with_residual=with_residual)
+        ref = oracle.Oracle().reduce_rmsnorm_quant(inp.partials, inp.residual, inp.gamma, inp.eps, 128,
+                                                   threads=THREADS)
+        _CACHE[key] = (inp, DevInputs(inp), ref)
+    return _CACHE[key]
+
+
+@pytest.mark.parametrize("with_residual", [True, False], ids=["residual", "no_residual"])
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_two_stage_norm_against_oracle(name, with_residual):
+    """reduce -> residual add + RMSNorm, element by element against the oracle."""
+    inp, d, (rro, ry, _, _) = _workload(name, with_residual)
+    y, ro = frn.unfused_reduce_rmsnorm(d.partials, d.residual, d.gamma, inp.eps, stages=2)
+    assert_residual_exact(host_bits(ro), rro, f"2-stage norm {name}")
+    assert_y_close(host_bits(y), ry, f"2-stage norm {name}")
+
+
+@pytest.mark.parametrize("with_residual", [True, False], ids=["residual", "no_residual"])
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+@pytest.mark.parametrize("stages", [2, 3])
+@pytest.mark.parametrize("emit", [True, False], ids=["B", "A"])
+def test_quant_paths_against_oracle(name, with_residual, stages, emit):
+    """2 kernels (fused reduce + RMSNorm -> stand-alone per-group quant) and 3
+    kernels (reduce -> add + RMSNorm -> quant), both output variants, element by
+    element against the oracle."""
+    inp, d, (rro, ry, rq, rs) = _workload(name, with_residual)
+    out, ro = frn.unfused_reduce_rmsnorm(d.partials, d.residual, d.gamma, inp.eps, stages=stages, quant=True,
+                                         emit_bf16=emit)
+    what = f"{stages}-stage quant {'B' if emit else 'A'} {name}"
+    assert_residual_exact(host_bits(ro), rro, what)
+    y = host_bits(out[0]) if emit else None
+    if emit:
+        assert_y_close(y, ry, what)
+    assert_quant_close(y, host_bits(out[-2]), host_bits(out[-1]), ry, rq, rs, what)
 
 
 def test_unfused_against_oracle_no_residual():
