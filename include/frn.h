@@ -260,7 +260,8 @@ frn_status frn_unfused_reduce_rmsnorm_noalloc(const void* const* partials, int R
  *           dst0 and dst1 -- the traffic of a call without quant (R partials
  *           and the residual in; residual_out and y out) without its arithmetic.
  * Kinds 1 and 2 launch ceil(nbytes / 16 / threads) CTAs (grid_ctas unused).
- * threads: a multiple of 32 in 32..1024.  All pointers 16-byte aligned.
+ * threads: a multiple of 32, up to 1024 for kind 0 and 512 for kinds 1 and 2.
+ * All pointers 16-byte aligned.
  * Returns FRN_ERR_INVALID_ARG / FRN_ERR_MISALIGNED without launching on bad
  * arguments, FRN_ERR_CUDA on a launch error; frn_last_error_detail is not set.
  */

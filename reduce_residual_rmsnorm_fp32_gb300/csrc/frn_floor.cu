@@ -37,8 +37,9 @@ __global__ void frn_floor_empty_kernel() {
     launch_dependents();
 }
 
+// up to 512 threads: the 17 source vectors stay in registers (no spills)
 template <bool WRITE>
-__global__ void __launch_bounds__(1024) frn_floor_copy_kernel(const __grid_constant__ FloorParams p) {
+__global__ void __launch_bounds__(512) frn_floor_copy_kernel(const __grid_constant__ FloorParams p) {
     grid_dependency_wait();
     const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     const bool valid = i < p.nvec;
@@ -78,7 +79,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 FRN_EXPORT frn_status frn_floor_launch(int kind, const void* const* srcs, int n_src, void* dst0, void* dst1,
                                        int64_t nbytes, int threads, int64_t grid_ctas, int pdl,
                                        frn_stream_t stream) {
-    if (kind < 0 || kind > 2 || threads < 32 || threads > 1024 || threads % 32 != 0) return FRN_ERR_INVALID_ARG;
+    if (kind < 0 || kind > 2 || threads < 32 || threads > (kind == 0 ? 1024 : 512) || threads % 32 != 0)
+        return FRN_ERR_INVALID_ARG;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);

@@ -131,7 +131,9 @@ def assert_mx_close(y_gpu, q_gpu, s_gpu, y_ref, q_ref, s_ref, what="") -> int:
     if y_gpu is not None:
         same = np.all(y_gpu.reshape(T, H // 32, 32) == y_ref.reshape(T, H // 32, 32), axis=-1)
     else:
-        same = s_gpu == s_ref
+        # without the GPU's y, a block whose y flipped by one ulp shows only as a
+        # differing code or scale: such blocks are counted below
+        same = (s_gpu == s_ref) & np.all(c == rc, axis=-1)
     assert np.array_equal(s_gpu[same], s_ref[same]), what
     assert np.array_equal(c[same], rc[same]), what
     dc = np.abs(ordered_e2m1(c) - ordered_e2m1(rc))

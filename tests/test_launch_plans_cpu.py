@@ -40,6 +40,7 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
         if C > 1:                                                          # cluster variant: <= 512 threads
             assert thr <= 512 and rows == 1 and C <= 8, what
         assert pl["grid"] == -(-T // rows) * C, what
+        assert pl["smem_bytes"] == 0, what
     else:
         tpw, nc, g, slots = pl["tiles_per_warp"], pl["consumer_warps"], pl["groups"], pl["slots"]
         nslices = R + (1 if residual else 0)
