@@ -7,9 +7,11 @@ is effective GB/s -- algorithmic HBM bytes of the step over its device time --
 next to its fraction of the measured HBM peak, plus microseconds per call at
 each decode T.  Each step reads a different one of several rotating input
 sets whose total size exceeds twice the L2, so no step hits inputs the previous
-one left in L2.  Steps run as CUDA-graph replays: one graph holds one step per
-input set (four launches each), as a decode engine's graph holds the epilogues
-of all its layers.
+one left in L2.  Steps run as CUDA-graph replays, four launches a step, as a
+decode engine's graph holds the epilogues of all its layers: the K timed steps
+are one graph of exactly K steps (for K up to 2048; beyond, replays of a graph
+of one pass over the sets plus one graph of the rest), so the result does not
+depend on K.
 
 Besides the JSON contract keys, the line carries:
   decode_us_per_call  per T: graph replay and raw (Python-launched) calls;
@@ -741,8 +743,8 @@ def main():
 
     # ---- headline: decode steps over rotating input sets, as graph replays.
     # One graph holds one step per input set, in order (as a decode graph holds
-    # the epilogues of all its layers); single-step graphs run the remainder
-    # when the step count is not a multiple of the set count.
+    # the epilogues of all its layers); one graph of exactly that many steps
+    # runs the remainder when the step count is not a multiple of the set count.
     per_set = sum(syn.algorithmic_bytes(R_DEC, T, H, "norm") for T in DECODE_T)
     nsets = max(16, sets_to_beat_l2(per_set))
     gamma = syn.make_inputs_device(1, 1, H, seed=3)[2]
@@ -752,42 +754,63 @@ def main():
         for st in sets:
             st.step(frn)
     chain = capture(all_sets)
+    # The timed region is one graph launch of exactly K steps (the sets in
+    # rotation) when K is at most ONE_GRAPH_MAX; beyond that, K // nsets
+    # replays of the chain and one graph of the remaining steps, whose single
+    # switch between graphs is then spread over more than ONE_GRAPH_MAX steps.
+    # Every graph is launched once before the timed region (a first launch
+    # uploads it), and the launch right before the start event is of the same
+    # graph as the timed one.
+    ONE_GRAPH_MAX = 2048
     tails = {}
 
     def tail(k):
-        """A graph of the first k steps of a pass, captured ahead of the timed region."""
+        """A graph of k steps, the sets in rotation, captured ahead of the timed region."""
         if k not in tails:
-            tails[k] = capture(lambda: [sets[i].step(frn) for i in range(k)])
+            tails[k] = capture(lambda: [sets[i % nsets].step(frn) for i in range(k)])
         return tails[k]
-    for k in {args.steps % nsets, args.warmup % nsets} - {0}:
-        tail(k)
+
+    def plan(n):
+        if n <= ONE_GRAPH_MAX:
+            return [(tail(n), 1)] if n else []
+        parts = [(chain, n // nsets)]
+        if n % nsets:
+            parts.append((tail(n % nsets), 1))
+        return parts
+
+    for g, _ in plan(args.steps) + plan(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
 
     def run_steps(n):
-        """n steps: whole passes as replays of the chain graph, the rest as one
-        graph of exactly that many steps, so every step runs the same way."""
-        for _ in range(n // nsets):
-            chain.replay()
-        if n % nsets:
-            tail(n % nsets).replay()
+        for g, reps in plan(n):
+            for _ in range(reps):
+                g.replay()
 
     # clocks are sampled from here to the end of the timed region: a ~0.5 s
     # stretch of the same steps first (part of the warm-up), then the timed steps
     sampler = ClockSampler(local)
     sampler.start()
+    # (the timed region's own graphs replayed over and over: a graph's first
+    # few launches run slower than later ones)
     t_end = time.perf_counter() + 0.5
     run_steps(args.warmup)
-    while time.perf_counter() < t_end:
-        run_steps(256 * nsets)
+    reps = 0
+    while time.perf_counter() < t_end or reps < 3:
+        run_steps(max(args.steps, nsets))
         torch.cuda.synchronize()
+        reps += 1
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # One more untimed pass, enqueued just before the start event: the GPU runs
-    # it while the host enqueues the timed graphs, so the events bracket the
-    # device time of exactly the K timed steps, not the host's latency to
-    # submit the first graph to an idle GPU.
-    chain.replay()
+    # One more untimed launch of the timed region's first graph, enqueued just
+    # before the start event: the GPU runs it while the host enqueues the timed
+    # graphs, so the events bracket the device time of exactly the K timed
+    # steps, not the host's latency to submit the first graph to an idle GPU.
+    timed = plan(args.steps)
+    if timed:
+        timed[0][0].replay()
     e0.record()
     run_steps(args.steps)
     e1.record()
@@ -845,9 +868,12 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded torch.randn on device, bf16 inputs)",
         "config": {"workload": WORKLOAD, "R": R_DEC, "H": H, "T": list(DECODE_T),
-                   "launch": f"CUDA graph replay, one graph per pass over the {nsets} input sets "
-                             f"({nsets} steps, {nsets * len(DECODE_T)} kernels), the remaining "
-                             f"steps % {nsets} as one graph of exactly that many steps",
+                   "launch": (f"CUDA graph replay: one graph of exactly {args.steps} steps over the "
+                              f"{nsets} input sets in rotation ({args.steps * len(DECODE_T)} kernels)"
+                              if args.steps <= ONE_GRAPH_MAX else
+                              f"CUDA graph replay: {args.steps // nsets} replays of one graph per pass over "
+                              f"the {nsets} input sets ({nsets * len(DECODE_T)} kernels), then one graph of "
+                              f"the remaining {args.steps % nsets} steps"),
                    "l2": f"{nsets} rotating input sets, {nsets * per_set / 1e6:.0f} MB > 2x L2 "
                          f"({l2_bytes() / 1e6:.0f} MB)", "parallelism": f"replicas x{world}"},
         "frac_of_hbm": round(value / world / hbm, 4), "hbm_peak_gbs": hbm, "hbm_peak_kind": peak_kind,
