@@ -399,6 +399,19 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // cluster CTAs.  Measured on GB300: below that, and for packed short rows
 // (up to 2x slower at H = 256), the extra requests cost more than the overlap
 // gives; beyond two waves it gains nothing.
+// CTAs of a row-kernel launch resident on one SM: by threads (2048), CTAs
+// (32) and the registers the kernel's launch bound holds (row_min_blocks).
+long long row_ctas_per_sm(const frn::RowPlan& plan, int R) {
+    const bool cluster = plan.ctas_per_row > 1;
+    const int maxt = plan.rows_per_cta > 1 ? frn::kPackedThreads : (plan.threads > frn::kMaxThreads ? 1024 : frn::kMaxThreads);
+    const int rmax = R <= 1 ? 1 : R <= 2 ? 2 : R <= 4 ? 4 : R <= 8 ? 8 : 16;
+    int by_regs = frn::row_min_blocks(rmax, cluster, maxt);
+    if (by_regs < 1) by_regs = 1;
+    long long n = 2048 / plan.threads;
+    if (n > 32) n = 32;
+    return n < by_regs ? n : by_regs;
+}
+
 bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms) {
     if (plan.grid * plan.threads > 2048LL * sms || plan.rows_per_cta > 1) return false;
     const long long row_bytes = 2LL * H * (R + 1);
@@ -425,17 +438,15 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // T = 8192, H = 7168, R = 2; +2% at T = 32, where it is left off).
     p.rstd_one_warp = kind == kRows && rplan.grid * rplan.threads > 2048LL * sms;
     // More rows than one wave holds, with R <= 2 (few loads in flight per SM):
-    // each CTA prefetches the row about one wave ahead (the CTAs resident at
-    // 2048 threads an SM).  Measured on GB300 at H = 7168: +6% at T = 8192
-    // without quant, +4..5% at T = 512..1024; -1% for a y-less quant at
-    // T = 8192 (issue-bound there), so it is left out for those beyond four
-    // waves; with R >= 4 it cost 8..17% (enough loads in flight already).
+    // each CTA prefetches its span of the rows about one wave ahead (the CTAs
+    // resident an SM by threads and by the registers the launch bound holds),
+    // one bulk request per input.  Measured on GB300 at R = 2, H = 7168: +6%
+    // at T = 8192 without quant, +4..5% at T = 512..1024; at T = 8192 FP8 A
+    // 92.1 -> 86.0 us, MXFP4 A 86.0 -> 79.9 us (a request per warp and input
+    // instead measured -1% there).
     if (kind == kRows && pf != 1 && c.R <= 2) {
-        const long long wave_rows =
-            static_cast<long long>(2048 / rplan.threads) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
-        const bool yless_quant = quant == 1 || quant == 3;
-        if (wave_rows > 0 && c.T > wave_rows && (!yless_quant || c.T <= 4 * wave_rows))
-            p.prefetch_ahead = wave_rows;
+        const long long wave_rows = row_ctas_per_sm(rplan, c.R) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
+        if (wave_rows > 0 && c.T > wave_rows) p.prefetch_ahead = wave_rows;
     }
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -41,6 +41,26 @@ __device__ __forceinline__ void prefetch_tile_span(const Params& p, long long ro
     if (src != nullptr) bulk_prefetch_l2(src, 16u * static_cast<uint32_t>(nv));
 }
 
+// Lanes 0..R-1 of the CTA's first warp ask for the CTA's span of each partial
+// of row `row0` to be fetched into L2, lane R for the residual's: one bulk
+// prefetch of up to a row per input (for packed short rows, `nrows` whole
+// consecutive rows).  Used for the prefetch one wave ahead, where a few large
+// requests cost the issuing warps less than a request per warp and input.
+// Hints only: nothing reads a value from them.
+__device__ __forceinline__ void prefetch_cta_span(const Params& p, long long row0, int nrows, int tile0, int lane) {
+    if (lane > p.R) return;
+    const uint4* base = lane < p.R ? p.partials[lane] : p.residual;
+    if (base == nullptr) return;
+    base += row0 * static_cast<long long>(p.nvec);
+    if (nrows > 1) {
+        bulk_prefetch_l2(base, 16u * static_cast<uint32_t>(nrows * p.nvec));
+        return;
+    }
+    const int first = tile0 * kTileVecs;
+    const int end = (tile0 + p.tiles_per_cta) * kTileVecs < p.nvec ? (tile0 + p.tiles_per_cta) * kTileVecs : p.nvec;
+    if (end > first) bulk_prefetch_l2(base + first, 16u * static_cast<uint32_t>(end - first));
+}
+
 // RMAX is the unrolled partial count (R <= RMAX; loads beyond R are predicated
 // off).  CLUSTER == false is the single-CTA row (no cluster barriers).  MAXT is
 // the launch bound: 512 threads (16 tiles), 1024 for a single-CTA row of up
@@ -108,10 +128,17 @@ frn_row_kernel(const __grid_constant__ Params p) {
     // previous kernel's writes land, so every value read after the wait below
     // is still the completed one.
     if (p.prefetch_l2 && tile < p.ntiles && in_rows) prefetch_tile_span(p, row, tile, lane, true);
-    // Many rows: ask for the same tile of the row about one wave of CTAs ahead,
-    // so that the CTA which takes that row finds it in L2.
-    if (p.prefetch_ahead > 0 && tile < p.ntiles && row + p.prefetch_ahead < p.T)
-        prefetch_tile_span(p, row + p.prefetch_ahead, tile, lane, false);
+    // Many rows: ask for this CTA's span of the rows about one wave of CTAs
+    // ahead, so that the CTA which takes them finds them in L2.
+    if (p.prefetch_ahead > 0 && warp == 0) {
+        const long long row0 = kPacked ? static_cast<long long>(blockIdx.x) * p.rows_per_cta : row;
+        const long long ahead = row0 + p.prefetch_ahead;
+        if (ahead < p.T) {
+            const long long left = p.T - ahead;
+            const int nrows = kPacked ? static_cast<int>(left < p.rows_per_cta ? left : p.rows_per_cta) : 1;
+            prefetch_cta_span(p, ahead, nrows, rank * p.tiles_per_cta, lane);
+        }
+    }
 
     // Nothing of the previous kernel on the stream may be read (or overwritten)
     // before it has completed.
