@@ -42,16 +42,19 @@ __device__ __forceinline__ void prefetch_tile_span(const Params& p, long long ro
 }
 
 // Lanes 0..R-1 of the CTA's first warp ask for the CTA's span of each partial
-// of row `row0` to be fetched into L2, lane R for the residual's: one bulk
-// prefetch of up to a row per input (for packed short rows, `nrows` whole
-// consecutive rows).  Used for the prefetch one wave ahead, where a few large
+// of row `row0` to be fetched into L2, lane R for the residual's, lane R+1 for
+// gamma's (when with_gamma): one bulk prefetch of up to a row per input (for
+// packed short rows, `nrows` whole consecutive rows).  Used for the prefetch
+// one wave ahead and for a cluster CTA's slice of its row, where a few large
 // requests cost the issuing warps less than a request per warp and input.
 // Hints only: nothing reads a value from them.
-__device__ __forceinline__ void prefetch_cta_span(const Params& p, long long row0, int nrows, int tile0, int lane) {
-    if (lane > p.R) return;
-    const uint4* base = lane < p.R ? p.partials[lane] : p.residual;
+__device__ __forceinline__ void prefetch_cta_span(const Params& p, long long row0, int nrows, int tile0, int lane,
+                                                  bool with_gamma = false) {
+    if (lane > p.R + (with_gamma ? 1 : 0)) return;
+    const uint4* base = lane < p.R ? p.partials[lane] : lane == p.R ? p.residual : p.gamma;
     if (base == nullptr) return;
-    base += row0 * static_cast<long long>(p.nvec);
+    if (lane <= p.R) base += row0 * static_cast<long long>(p.nvec);
+    else nrows = 1;
     if (nrows > 1) {
         bulk_prefetch_l2(base, 16u * static_cast<uint32_t>(nrows * p.nvec));
         return;
@@ -127,7 +130,16 @@ frn_row_kernel(const __grid_constant__ Params p) {
     // finishing.  A prefetch hands no value to this kernel, and L2 is where the
     // previous kernel's writes land, so every value read after the wait below
     // is still the completed one.
-    if (p.prefetch_l2 && tile < p.ntiles && in_rows) prefetch_tile_span(p, row, tile, lane, true);
+    if (p.prefetch_l2) {
+        // a cluster CTA's slice in one request per input (measured faster at
+        // decode T = 16 and 32, where rows are split over 4 and 2 CTAs); a
+        // whole-row CTA's by each warp for its own tile (faster for wide rows)
+        if constexpr (CLUSTER) {
+            if (warp == 0) prefetch_cta_span(p, row, 1, rank * p.tiles_per_cta, lane, true);
+        } else {
+            if (tile < p.ntiles && in_rows) prefetch_tile_span(p, row, tile, lane, true);
+        }
+    }
     // Many rows: ask for this CTA's span of the rows about one wave of CTAs
     // ahead, so that the CTA which takes them finds them in L2.
     if (p.prefetch_ahead > 0 && warp == 0) {
