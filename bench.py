@@ -27,7 +27,8 @@ Besides the JSON contract keys, the line carries:
                       with per-group FP8 quant (both output variants), without
                       quant and with MXFP4, each with effective GB/s and
                       fraction of HBM peak
-  sweep               all 12 message sizes, 32 KB .. 64 MB per partial
+  sweep               all 12 message sizes, 32 KB .. 64 MB per partial, each
+                      next to the copy reference kernel on the same buffers
   quant_R4_T32_H4096  the FP8 workload R=4, T=32, H=4096, both output variants
   fusion_gain         the fused call against the 2- and 3-kernel unfused paths
   roofline            the dominant kernel of the step (the T=64 call)
@@ -407,9 +408,10 @@ def measure_host_cost(frn, calls: int = 20000):
     return out
 
 
-def measure_rows(frn, R, T, mode, seed, hbm, outlier=False, partial_std=0.5, H=H):
+def measure_rows(frn, R, T, mode, seed, hbm, outlier=False, partial_std=0.5, H=H, copy_floor=False):
     """Effective GB/s of one call shape, cold L2 (rotating sets or inputs larger
-    than L2)."""
+    than L2); with copy_floor (no quant only), also the copy reference kernel's
+    time on the same buffers."""
     fp = syn.algorithmic_bytes(R, T, H, mode)
     n = sets_to_beat_l2(fp)
     sets = []
@@ -437,11 +439,24 @@ def measure_rows(frn, R, T, mode, seed, hbm, outlier=False, partial_std=0.5, H=H
                                                          y=y, q=q, scales=s)
     gr = capture(body)
     t = time_graph(gr, n, min_seconds=0.2)
-    del sets, gr
+    del gr
+    out = {"R": R, "T": T, "H": H, "mode": mode, "us": round(t * 1e6, 2), "bytes": fp,
+           "GBps": round(fp / t / 1e9, 1), "frac_of_hbm": round(fp / t / 1e9 / hbm, 4), "input_sets": n}
+    if copy_floor and mode == "norm":
+        # the copy reference kernel on the same buffers: the same bytes in and
+        # out, one 16-byte vector of every input per thread, no arithmetic
+        def floor_body():
+            for p, r, g, ro, y, q, s in sets:
+                frn.floor_launch(frn.FLOOR_COPY, [p[i] for i in range(R)] + [r], ro, y)
+        gf = capture(floor_body)
+        tf = time_graph(gf, n, min_seconds=0.2)
+        del gf
+        out["copy_floor_us"] = round(tf * 1e6, 2)
+        out["copy_floor_frac_of_hbm"] = round((fp - 2 * H) / tf / 1e9 / hbm, 4)
+        out["of_copy_floor"] = round(t / tf, 3)
+    del sets
     torch.cuda.empty_cache()
-    gbs = fp / t / 1e9
-    return {"R": R, "T": T, "H": H, "mode": mode, "us": round(t * 1e6, 2), "bytes": fp,
-            "GBps": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "input_sets": n}
+    return out
 
 
 def measure_fusion(frn, R, T, Hh, seed, hbm, outlier=False, partial_std=0.5):
@@ -845,7 +860,8 @@ def main():
         large.append(measure_rows(frn, 2, 8192, "mx_a", 33000, hbm, outlier=True, partial_std=1.0))
         large.append(measure_rows(frn, 2, 8192, "mx_b", 34000, hbm, outlier=True, partial_std=1.0))
         extras["large_T"] = large
-        extras["sweep"] = [dict(msg_bytes=m, **measure_rows(frn, 8, syn.sweep_tokens(m), "norm", 40000 + i, hbm))
+        extras["sweep"] = [dict(msg_bytes=m, **measure_rows(frn, 8, syn.sweep_tokens(m), "norm", 40000 + i, hbm,
+                                                             copy_floor=True))
                            for i, m in enumerate(syn.SWEEP_BYTES)]
         extras["quant_R4_T32_H4096"] = [measure_rows(frn, 4, 32, md, 50000, hbm, H=4096)
                                         for md in ("quant_a", "quant_b")]
