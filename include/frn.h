@@ -331,6 +331,9 @@ frn_status frn_set_stream_groups(int groups);
  *   groups, consumer_warps, slots, smem_bytes
  *                   stream kernel: consumer groups, warps a group, ring slots
  *                   (one 2*H-byte row slice each), dynamic shared memory
+ *   staged          row kernel: 1 when each thread loads its partials in
+ *                   stages of two (two stages in flight, 32 registers) rather
+ *                   than all at once, so that more rows share an SM
  * Launch controls (frn_set_kernel, frn_set_ctas_per_row, ...) apply as they
  * would to a call.
  */
@@ -346,6 +349,7 @@ typedef struct frn_launch_plan {
     int consumer_warps;
     int slots;
     int smem_bytes;
+    int staged;
 } frn_launch_plan;
 
 frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int has_residual, int num_sms,

@@ -163,7 +163,7 @@ class _LaunchPlan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("ctas_per_row", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
                 ("tiles_per_cta", ctypes.c_int), ("tiles_per_warp", ctypes.c_int), ("threads", ctypes.c_int),
                 ("grid", ctypes.c_int64), ("groups", ctypes.c_int), ("consumer_warps", ctypes.c_int),
-                ("slots", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+                ("slots", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("staged", ctypes.c_int)]
 
 
 def plan_launch(T: int, H: int, R: int, quant: int = 0, residual: bool = True, num_sms: int = 152) -> dict:

@@ -39,6 +39,7 @@ std::atomic<unsigned int*> g_status_addr[kMaxDevices];
 
 enum Kind : int { kAuto = 0, kRows = 1, kStream = 2 };
 
+
 frn_status fail(frn_status s, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -103,6 +104,7 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
     plan.rows_per_cta = 1;
     plan.threads = ntiles * 32;
     plan.grid = T;
+    plan.staged = 0;
     return plan;
 }
 
@@ -162,6 +164,33 @@ frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     if (C == 1 && ntiles <= 4 && T >= 4LL * num_sms) plan.rows_per_cta = 8 / ntiles;
     plan.threads = plan.rows_per_cta * tpc * 32;
     plan.grid = (T + plan.rows_per_cta - 1) / plan.rows_per_cta * C;
+    plan.staged = 0;
+    return plan;
+}
+
+// Staged partial loads for a one-CTA row (two stages of two loads in flight,
+// 32 registers, so that two to four rows share an SM) where they measured
+// faster on GB300, each only once the grid is several waves of the
+// all-loads-at-once kernel (below that the second DRAM round trip of a row
+// shows: R = 16, H = 4096, T = 293: 10.6 vs 9.6 us):
+//  * R > 8 (rows of <= 16 tiles; 96 registers otherwise, one row per SM) from
+//    three waves: R = 16, H = 4096, T = 586 / 1171 / 4096: 16.8 / 29.7 / 95.8 us
+//    against 18.8 / 33.8 / 99.9 us;
+//  * R = 5..8 wide rows with a quant output at three to six waves, where they
+//    also beat the stream kernel: R = 8, H = 7168, T = 586: FP8 A 17.9 vs 19.5
+//    (stream 19.7) us, FP8 B 19.0 vs 21.0 (20.8), MXFP4 A 16.9 vs 18.8 (17.5);
+//    at T = 293 and from T = 1171 on they measured no better.
+bool staged_window(long long T, int H, int R, int quant, int num_sms) {
+    const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
+    if (R > 8) return ntiles <= frn::kMaxTilesPerCta && T >= 3LL * num_sms;
+    return quant != 0 && R >= 5 && ntiles > frn::kMaxTilesPerCta && wide_possible(ntiles, R) &&
+           T >= 3LL * num_sms && T < 6LL * num_sms;
+}
+
+frn::RowPlan plan_rows(long long T, int H, int R, int quant, int num_sms) {
+    frn::RowPlan plan = choose_rows(T, H, R, num_sms);
+    if (plan.ctas_per_row == 1 && plan.rows_per_cta == 1 && staged_window(T, H, R, quant, num_sms))
+        plan.staged = 1;
     return plan;
 }
 
@@ -210,13 +239,13 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
 //    H = 7168: 68 vs 81 us at T = 4096);
 //  * a wider row: the stream kernel from one row per SM on.
 int choose_kind(long long T, int H, int R, int quant, int num_sms) {
-    (void)quant;
     const int forced = g_force_kernel.load(std::memory_order_relaxed);
     if (forced == kRows || forced == kStream) return forced;
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
     if (ntiles <= frn::kMaxTilesPerCta) return kRows;
     if (wide_possible(ntiles, R)) {
         if (T < 2LL * num_sms) return kRows;
+        if (staged_window(T, H, R, quant, num_sms)) return kRows;
         // two or more wide rows resident per SM (threads, and the registers the
         // launch bound holds: 32 for R <= 2, 48 for R <= 4, 64 for R <= 8)
         const int threads = ntiles * 32;
@@ -421,7 +450,7 @@ bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms)
 
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
+    const frn::RowPlan rplan = plan_rows(c.T, c.H, c.R, quant, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
@@ -740,13 +769,14 @@ FRN_EXPORT frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int ha
         out->threads = (plan.groups * plan.consumer_warps + 1) * 32;
         out->grid = plan.grid;
     } else {
-        const frn::RowPlan plan = choose_rows(T, H, R, num_sms);
+        const frn::RowPlan plan = plan_rows(T, H, R, quant, num_sms);
         out->ctas_per_row = plan.ctas_per_row;
         out->rows_per_cta = plan.rows_per_cta;
         out->tiles_per_warp = 1;
         out->tiles_per_cta = plan.tiles_per_cta;
         out->threads = plan.threads;
         out->grid = plan.grid;
+        out->staged = plan.staged;
     }
     return ok();
 }

@@ -76,16 +76,23 @@ __device__ __forceinline__ void prefetch_cta_span(const Params& p, long long row
 // what the compiler picks.
 constexpr int kPackedThreads = 256;   // the packed short-row variant
 
-constexpr int row_min_blocks(int rmax, bool cluster, int maxt) {
-    return cluster ? 1
+constexpr int row_min_blocks(int rmax, bool cluster, int maxt, bool staged = false) {
+    return staged ? (maxt > kMaxThreads ? 2 : 4)
+         : cluster ? 1
          : maxt > kMaxThreads ? (rmax <= 2 ? 2 : 1)
          : maxt == kPackedThreads ? (rmax <= 2 ? 8 : rmax <= 4 ? 6 : rmax <= 8 ? 4 : 2)
                                   : (rmax <= 2 ? 4 : rmax <= 4 ? 3 : rmax <= 8 ? 2 : 1);
 }
 
-template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
-__global__ void __launch_bounds__(MAXT, row_min_blocks(RMAX, CLUSTER, MAXT))
+// STAGED (single-CTA rows, RMAX 8 or 16): a thread keeps two stages of two
+// partial loads in flight instead of all R at once, and sums them in rank
+// order as they arrive, so that it fits 32 registers -- two rows of up to 8192
+// elements resident per SM instead of one, which keeps loads in flight while
+// the other row runs its epilogue.
+template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads, bool STAGED = false>
+__global__ void __launch_bounds__(MAXT, row_min_blocks(RMAX, CLUSTER, MAXT, STAGED))
 frn_row_kernel(const __grid_constant__ Params p) {
+    static_assert(!STAGED || (!CLUSTER && MAXT != 256 && RMAX % 4 == 0), "staged loads: single-CTA rows");
     // MAXT == 256 (single CTA only): several short rows per CTA, ntiles warps each
     constexpr bool kPacked = !CLUSTER && MAXT == kPackedThreads;
     // single CTA: this CTA's tile sums; cluster: every tile sum of the row
@@ -156,20 +163,48 @@ frn_row_kernel(const __grid_constant__ Params p) {
     // before it has completed.
     grid_dependency_wait();
 
-    uint4 raw[RMAX];
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) raw[r] = ld_stream(p.partials[r] + off, valid && r < p.R);
-    const uint4 res = ld_coherent(p.residual + off, valid && p.residual != nullptr);
-    const uint4 g = ld_keep(p.gamma + j, valid);
-    launch_dependents();
-
     // fp32 sum in rank order, residual last (+0 when absent), one RNE to bf16.
     float acc[8];
-    unpack8(raw[0], acc);
+    uint4 g;
+    if constexpr (STAGED) {
+        // stages (a, b) of two partials each: issue the next stage, then add
+        // the one before it
+        uint4 a0 = ld_stream(p.partials[0] + off, valid);
+        uint4 a1 = ld_stream(p.partials[1] + off, valid && 1 < p.R);
+        uint4 b0 = ld_stream(p.partials[2] + off, valid && 2 < p.R);
+        uint4 b1 = ld_stream(p.partials[3] + off, valid && 3 < p.R);
+        launch_dependents();
+        unpack8(a0, acc);
+        if (1 < p.R) add8(acc, a1);
 #pragma unroll
-    for (int r = 1; r < RMAX; ++r)
-        if (r < p.R) add8(acc, raw[r]);
-    add8(acc, res);
+        for (int r = 4; r < RMAX; r += 4) {
+            a0 = ld_stream(p.partials[r] + off, valid && r < p.R);
+            a1 = ld_stream(p.partials[r + 1] + off, valid && r + 1 < p.R);
+            if (r - 2 < p.R) add8(acc, b0);
+            if (r - 1 < p.R) add8(acc, b1);
+            b0 = ld_stream(p.partials[r + 2] + off, valid && r + 2 < p.R);
+            b1 = ld_stream(p.partials[r + 3] + off, valid && r + 3 < p.R);
+            if (r < p.R) add8(acc, a0);
+            if (r + 1 < p.R) add8(acc, a1);
+        }
+        const uint4 res = ld_coherent(p.residual + off, valid && p.residual != nullptr);
+        g = ld_keep(p.gamma + j, valid);
+        if (RMAX - 2 < p.R) add8(acc, b0);
+        if (RMAX - 1 < p.R) add8(acc, b1);
+        add8(acc, res);
+    } else {
+        uint4 raw[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) raw[r] = ld_stream(p.partials[r] + off, valid && r < p.R);
+        const uint4 res = ld_coherent(p.residual + off, valid && p.residual != nullptr);
+        g = ld_keep(p.gamma + j, valid);
+        launch_dependents();
+        unpack8(raw[0], acc);
+#pragma unroll
+        for (int r = 1; r < RMAX; ++r)
+            if (r < p.R) add8(acc, raw[r]);
+        add8(acc, res);
+    }
     const uint4 ro = pack8(acc);
 
     const float s = tile_sumsq(ro);
@@ -286,9 +321,10 @@ struct RowPlan {
     int rows_per_cta;   // single-CTA rows only: short rows share a CTA
     int threads;
     long long grid;
+    int staged;         // single-CTA rows with R >= 3: staged partial loads (STAGED)
 };
 
-template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads>
+template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads, bool STAGED = false>
 cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
     if constexpr (CLUSTER) {
         if (plan.ctas_per_row > 8) {
@@ -298,7 +334,7 @@ cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t st
             cudaError_t e = cudaGetDevice(&dev);
             if (e != cudaSuccess) return e;
             if (dev < 0 || dev >= 64 || !opted[dev].load(std::memory_order_acquire)) {
-                e = cudaFuncSetAttribute(frn_row_kernel<RMAX, MODE, CLUSTER, MAXT>,
+                e = cudaFuncSetAttribute(frn_row_kernel<RMAX, MODE, CLUSTER, MAXT, STAGED>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (e != cudaSuccess) return e;
                 if (dev >= 0 && dev < 64) opted[dev].store(1, std::memory_order_release);
@@ -326,12 +362,18 @@ cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t st
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, frn_row_kernel<RMAX, MODE, CLUSTER, MAXT>, p);
+    return cudaLaunchKernelEx(&cfg, frn_row_kernel<RMAX, MODE, CLUSTER, MAXT, STAGED>, p);
 }
 
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
+    if (plan.staged) {
+        // one CTA per row, R >= 3 (R <= 8 for a wide CTA)
+        if (plan.threads > kMaxThreads) return launch_row_one<8, MODE, false, 1024, true>(p, plan, stream, pdl);
+        if (p.R <= 8) return launch_row_one<8, MODE, false, kMaxThreads, true>(p, plan, stream, pdl);
+        return launch_row_one<16, MODE, false, kMaxThreads, true>(p, plan, stream, pdl);
+    }
     if (plan.threads > kMaxThreads) {
         // one wide CTA per row (the host only plans this for R <= 8)
         if (p.R <= 1) return launch_row_one<1, MODE, false, 1024>(p, plan, stream, pdl);

@@ -41,6 +41,9 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
             assert thr <= 512 and rows == 1 and C <= 8, what
         assert pl["grid"] == -(-T // rows) * C, what
         assert pl["smem_bytes"] == 0, what
+        if pl["staged"]:                                                   # staged loads: one CTA a row
+            assert C == 1 and rows == 1 and R >= 5 and T >= 3 * sms, what
+            assert (R > 8 and ntiles <= 16) or (quant and thr > 512 and T < 6 * sms), what
     else:
         tpw, nc, g, slots = pl["tiles_per_warp"], pl["consumer_warps"], pl["groups"], pl["slots"]
         nslices = R + (1 if residual else 0)
@@ -124,3 +127,18 @@ def test_query_launch_checks_sizes_then_needs_a_device():
         assert lib.frn_query_launch(*bad, 1, ctypes.byref(k), None, None, None) == frn.FRN_ERR_INVALID_ARG
     if not torch.cuda.is_available():
         assert lib.frn_query_launch(8, 7168, 8, 0, 0, ctypes.byref(k), None, None, None) == frn.FRN_ERR_CUDA
+
+
+def test_staged_plans():
+    """Staged partial loads where they measured faster: R > 8 rows of up to 16
+    tiles from three waves; R = 5..8 wide rows with a quant output at three to
+    six waves (there the row kernel, not the stream kernel)."""
+    pl = frn.plan_launch(600, 4096, 16, 0, True, 152)
+    assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 1 and pl["threads"] == 512
+    assert frn.plan_launch(300, 4096, 16, 0, True, 152)["staged"] == 0
+    for quant in (1, 2, 3, 4):
+        pl = frn.plan_launch(586, 7168, 8, quant, True, 152)
+        assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 1 and pl["threads"] == 896
+        assert frn.plan_launch(1171, 7168, 8, quant, True, 152)["kernel"] == frn.KERNEL_STREAM
+    assert frn.plan_launch(586, 7168, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
+    assert frn.plan_launch(586, 7168, 4, 1, True, 152)["staged"] == 0

@@ -46,7 +46,8 @@ def kernel(request):
 
 
 @pytest.mark.parametrize("R,T,H", [(2, 4, 256), (8, 64, 7168), (4, 32, 4096), (3, 17, 1024), (1, 5, 32),
-                                   (16, 3, 16384), (2, 300, 7168), (2, 700, 256), (8, 650, 1024)])
+                                   (16, 3, 16384), (2, 300, 7168), (2, 700, 256), (8, 650, 1024), (8, 586, 7168),
+                                   (16, 600, 4096)])
 def test_mxfp4_parity(R, T, H, kernel):
     check_mx(syn.make_inputs(R, T, H, seed=R + T + H, partial_std=0.5), f"mx R={R} T={T} H={H} k={kernel}")
 

@@ -354,3 +354,28 @@ def test_stream_consumer_groups(groups, R, T, H):
     finally:
         frn.set_stream_groups(0)
         frn.set_kernel(frn.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("R,T,H", [(16, 600, 4096), (9, 500, 2048), (8, 586, 7168), (5, 500, 7168), (7, 470, 7936),
+                                   (12, 460, 1024)])
+def test_staged_loads(R, T, H):
+    """Rows whose partials are loaded in stages (two stages of two in flight),
+    as the planner picks them: every row of every output against the oracle,
+    and the same bits as the stream kernel."""
+    quant = H % 128 == 0
+    plan = frn.plan_launch(T, H, R, 1 if quant else 0, True,
+                           torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["staged"] == 1, plan
+    inp = syn.make_inputs(R, T, H, seed=40 + R + T, partial_std=0.5)
+    got = check_quant(inp, f"staged R={R} T={T} H={H}") if quant else check_norm(inp, f"staged R={R} T={T} H={H}")
+    d = DevInputs(inp)
+    outs = [gpu_quant(d, True), gpu_quant(d, False)] if quant else [gpu_norm(d)]
+    frn.set_kernel(frn.KERNEL_STREAM)
+    try:
+        ref = [gpu_quant(d, True), gpu_quant(d, False)] if quant else [gpu_norm(d)]
+    finally:
+        frn.set_kernel(frn.KERNEL_AUTO)
+    for a_set, b_set in zip(outs, ref):
+        for a, b in zip(a_set, b_set):
+            if a is not None:
+                assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
