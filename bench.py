@@ -689,6 +689,8 @@ PROFILE_CASES = {
     # name: (R, T, H, mode, outliers, partial_std)
     "decode64": (8, 64, H, "norm", False, 0.5),
     "decode8": (8, 8, H, "norm", False, 0.5),
+    "decode16": (8, 16, H, "norm", False, 0.5),
+    "staged_quant_a": (8, 586, H, "quant_a", False, 0.5),
     "sweep64M": (8, syn.sweep_tokens(64 << 20), H, "norm", False, 0.5),
     "sweep16M": (8, syn.sweep_tokens(16 << 20), H, "norm", False, 0.5),
     "prefill_quant_a": (2, 8192, H, "quant_a", True, 1.0),
