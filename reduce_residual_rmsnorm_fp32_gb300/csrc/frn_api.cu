@@ -237,7 +237,8 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
 //    55 us at R = 4, T = 4096, H = 5120), else the stream kernel, whose overlap
 //    of one row's epilogue with the next rows' loads then wins (R = 3..4 at
 //    H = 7168: 68 vs 81 us at T = 4096);
-//  * a wider row: the stream kernel from one row per SM on.
+//  * a wider row: the stream kernel from one row per SM on, the row kernel's
+//    clusters with an FP8 output.
 int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     const int forced = g_force_kernel.load(std::memory_order_relaxed);
     if (forced == kRows || forced == kStream) return forced;
@@ -253,6 +254,13 @@ int choose_kind(long long T, int H, int R, int quant, int num_sms) {
         const int by_threads = 2048 / threads, by_regs = 65536 / (threads * regs);
         return (by_threads < by_regs ? by_threads : by_regs) >= 2 ? kRows : kStream;
     }
+    // Wider rows: the stream kernel from one row per SM on -- except with an
+    // FP8 output, where its single consumer group's quant epilogue, which
+    // nothing overlaps, is slower than the row kernel's clusters (R = 2,
+    // T = 8192: H = 16384 FP8 A 266 vs 289 us, FP8 B 283 vs 287 us; H = 12288
+    // FP8 A 203 vs 220 us; R = 8, T = 2048, H = 16384 FP8 A 136 vs 151 us;
+    // without quant and with MXFP4 the stream kernel stays well ahead).
+    if (quant == 1 || quant == 2) return kRows;
     return T >= num_sms ? kStream : kRows;
 }
 

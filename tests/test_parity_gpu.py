@@ -379,3 +379,26 @@ def test_staged_loads(R, T, H):
         for a, b in zip(a_set, b_set):
             if a is not None:
                 assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
+@pytest.mark.parametrize("R,T,H", [(2, 300, 16384), (8, 200, 12288), (1, 170, 8320)])
+def test_wide_fp8_rows_on_clusters(R, T, H):
+    """FP8 output on rows wider than 8192: the planner takes the row kernel's
+    clusters (with R <= 2 and the one-wave-ahead prefetch); every row against
+    the oracle, and the same bits as the stream kernel."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = frn.plan_launch(T, H, R, 1, True, sms)
+    assert plan["kernel"] == frn.KERNEL_ROWS and plan["ctas_per_row"] > 1, plan
+    inp = syn.make_inputs(R, T, H, seed=60 + R, partial_std=0.5)
+    check_quant(inp, f"wide FP8 R={R} T={T} H={H}")
+    d = DevInputs(inp)
+    rows = [gpu_quant(d, True), gpu_quant(d, False)]
+    frn.set_kernel(frn.KERNEL_STREAM)
+    try:
+        stream = [gpu_quant(d, True), gpu_quant(d, False)]
+    finally:
+        frn.set_kernel(frn.KERNEL_AUTO)
+    for a_set, b_set in zip(rows, stream):
+        for a, b in zip(a_set, b_set):
+            if a is not None:
+                assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
