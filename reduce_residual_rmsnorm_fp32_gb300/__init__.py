@@ -202,6 +202,11 @@ def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, 
                   out: bool = False) -> None:
     """Inputs must be on the call's CUDA device; an output (out=True) may also be
     a pinned host tensor, which the kernel writes over the host link."""
+    # the common case, without building device objects; anything else takes the
+    # detailed checks below
+    if (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.get_device() == device.index
+            and t.shape == shape and t.is_contiguous()):
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device != device or device.type != "cuda":
@@ -216,6 +221,21 @@ def _check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, 
         raise ValueError(f"{name} must be contiguous")
 
 
+_tls = threading.local()
+
+
+def _pointer_array(ptrs: list[int]):
+    """The partial pointers as a C array of void* for the call.  One array per
+    thread, reused: the library copies the pointers during the call."""
+    buf = getattr(_tls, "ptrs", None)
+    if buf is None:
+        buf = _tls.ptrs = (ctypes.c_void_p * MAX_PARTIALS)()
+    if len(ptrs) > MAX_PARTIALS:
+        return (ctypes.c_void_p * len(ptrs))(*ptrs)   # the library rejects R > MAX_PARTIALS
+    buf[:len(ptrs)] = ptrs
+    return buf
+
+
 def _partials(partials) -> tuple[list[int], int, int, int, torch.device]:
     if isinstance(partials, torch.Tensor):
         if partials.dim() != 3:
@@ -224,7 +244,7 @@ def _partials(partials) -> tuple[list[int], int, int, int, torch.device]:
         dev = partials.device
         _check_tensor(partials, "partials", torch.bfloat16, (R, T, H), dev)
         base, step = partials.data_ptr(), T * H * 2
-        return [base + r * step for r in range(R)], R, T, H, dev
+        return list(range(base, base + R * step, step)) if step else [base] * R, R, T, H, dev
     parts = list(partials)
     if not parts:
         raise ValueError("partials is empty")
@@ -268,7 +288,7 @@ def fused_reduce_rmsnorm(partials: torch.Tensor | Sequence[torch.Tensor], residu
         y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     _check_tensor(residual_out, "residual_out", torch.bfloat16, (T, H), dev, out=True)
     _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
-    arr = (ctypes.c_void_p * R)(*ptrs)
+    arr = _pointer_array(ptrs)
     with _on(dev):
         st = library().fused_reduce_rmsnorm(arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y),
                                             T, H, float(eps), _stream(stream, dev))
@@ -306,7 +326,7 @@ def fused_reduce_rmsnorm_quant_per_group(partials, residual: torch.Tensor | None
         raise TypeError("q must be float8_e4m3fn or uint8")
     _check_tensor(q, "q", q.dtype, (T, H), dev, out=True)
     _check_tensor(scales, "scales", torch.float32, (T, H // group_size), dev, out=True)
-    arr = (ctypes.c_void_p * R)(*ptrs)
+    arr = _pointer_array(ptrs)
     with _on(dev):
         st = library().fused_reduce_rmsnorm_quant_per_group(
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales),
@@ -377,7 +397,7 @@ def unfused_reduce_rmsnorm(partials, residual: torch.Tensor | None, gamma: torch
         raise ValueError(f"workspace must be on {dev} (got {workspace.device})")
     if not workspace.is_contiguous():
         raise ValueError("workspace must be contiguous")
-    arr = (ctypes.c_void_p * R)(*ptrs)
+    arr = _pointer_array(ptrs)
     with _on(dev):
         st = library().frn_unfused_reduce_rmsnorm(
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q) if quant else None,
@@ -408,7 +428,7 @@ def unfused_reduce_rmsnorm_noalloc(partials, residual: torch.Tensor | None, gamm
     if (q is None) != (scales is None):
         raise ValueError("pass both q and scales (quant) or neither")
     _check_unfused_outputs(T, H, dev, q is not None, group_size, residual_out, y, q, scales)
-    arr = (ctypes.c_void_p * R)(*ptrs)
+    arr = _pointer_array(ptrs)
     with _on(dev):
         st = library().frn_unfused_reduce_rmsnorm_noalloc(
             arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y), _ptr(q), _ptr(scales), T, H,
@@ -503,7 +523,7 @@ def fused_reduce_rmsnorm_mxfp4(partials, residual: torch.Tensor | None, gamma: t
         _check_tensor(y, "y", torch.bfloat16, (T, H), dev, out=True)
     _check_tensor(q, "q", torch.uint8, (T, H // 2), dev, out=True)
     _check_tensor(scales, "scales", torch.uint8, (T, H // 32), dev, out=True)
-    arr = (ctypes.c_void_p * R)(*ptrs)
+    arr = _pointer_array(ptrs)
     with _on(dev):
         st = library().fused_reduce_rmsnorm_mxfp4(arr, R, _ptr(residual), _ptr(gamma), _ptr(residual_out), _ptr(y),
                                                   _ptr(q), _ptr(scales), T, H, float(eps), _stream(stream, dev))
