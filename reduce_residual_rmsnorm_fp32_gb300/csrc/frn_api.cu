@@ -702,7 +702,9 @@ FRN_EXPORT const char* frn_status_string(frn_status s) {
 
 FRN_EXPORT const char* frn_last_error_detail(void) { return g_detail; }
 
-FRN_EXPORT int frn_version(void) { return 100; }
+// 2.0.0: frn_query_launch takes has_residual; frn_launch_plan has `staged`;
+// frn_floor_launch added.
+FRN_EXPORT int frn_version(void) { return 20000; }
 
 FRN_EXPORT frn_status frn_set_l2_prefetch(int mode) {
     if (mode < 0 || mode > 2) return fail(FRN_ERR_INVALID_ARG, "l2 prefetch mode=%d must be 0..2", mode);
