@@ -110,8 +110,12 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
-// Ten waves of one-row-per-SM CTAs.
-long long many_waves(int num_sms) { return 10LL * num_sms; }
+// The row count from which wide rows with R >= 3 (one row per SM) take the row
+// kernel with its one-wave-ahead prefetch: seven waves for R >= 5 (R = 8,
+// H = 7168, T = 1171: no quant 31.9 vs 32.6 us, FP8 A 32.7 vs 34.1 us, FP8 B
+// 33.9 vs 36.1 us on the stream kernel), ten for R = 3, 4 (R = 4, T = 1171:
+// 22.1 vs 21.8 us; T = 2048: 34.8 vs 36.1 us).
+long long many_waves(int num_sms, int R) { return (R >= 5 ? 7LL : 10LL) * num_sms; }
 
 frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     const int nvec = H / frn::kVecElems;
@@ -250,12 +254,13 @@ int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     if (wide_possible(ntiles, R)) {
         if (T < 2LL * num_sms) return kRows;
         if (staged_window(T, H, R, quant, num_sms)) return kRows;
-        // From ten waves of one-per-SM rows on, the row kernel with its
-        // one-wave-ahead prefetch beats the stream kernel (R = 8, H = 7168:
-        // T = 2341 59.6 vs 62.5 us, T = 4682 109.8 vs 116.6 us; R = 4 / 5,
-        // T = 4096: 64.9 / 73.9 vs 68.4 / 78.5 us; FP8 A and MXFP4 B at
-        // T = 2341: 58.8 / 62.1 vs 60.2 / 65.2 us); below, the stream kernel.
-        if (T >= many_waves(num_sms)) return kRows;
+        // From seven (R >= 5) or ten waves of one-per-SM rows on, the row
+        // kernel with its one-wave-ahead prefetch beats the stream kernel
+        // (R = 8, H = 7168: T = 2341 59.6 vs 62.5 us, T = 4682 109.8 vs
+        // 116.6 us; R = 4 / 5, T = 4096: 64.9 / 73.9 vs 68.4 / 78.5 us; FP8 A
+        // and MXFP4 B at T = 2341: 58.8 / 62.1 vs 60.2 / 65.2 us); below, the
+        // stream kernel.
+        if (T >= many_waves(num_sms, R)) return kRows;
         // two or more wide rows resident per SM (threads, and the registers the
         // launch bound holds: 32 for R <= 2, 48 for R <= 4, 64 for R <= 8)
         const int threads = ntiles * 32;
@@ -490,11 +495,11 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // at T = 8192 without quant, +4..5% at T = 512..1024; at T = 8192 FP8 A
     // 92.1 -> 81.9 us, MXFP4 A 86.0 -> 76.6 us (a request per warp and input
     // instead measured -1% there).  With R >= 3 it pays only for wide rows
-    // (one row per SM) from ten waves on (R = 8, H = 7168, T = 4682: 115.0 ->
-    // 109.8 us with the row kernel); at two waves it cost 10 % (R = 8,
-    // T = 293), and 4 % for 512-thread rows.
+    // (one row per SM) at many waves (many_waves; R = 8, H = 7168, T = 4682:
+    // 115.0 -> 109.8 us with the row kernel); at two waves it cost 10 %
+    // (R = 8, T = 293), and 4 % for 512-thread rows.
     const bool wide_many = rplan.threads > frn::kMaxThreads && rplan.ctas_per_row == 1 && !rplan.staged &&
-                           c.T >= many_waves(sms);
+                           c.T >= many_waves(sms, c.R);
     if (kind == kRows && pf != 1 && (c.R <= 2 || wide_many)) {
         const long long wave_rows = row_ctas_per_sm(rplan, c.R) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
         if (wave_rows > 0 && c.T > wave_rows) p.prefetch_ahead = wave_rows;

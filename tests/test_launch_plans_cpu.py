@@ -139,6 +139,12 @@ def test_staged_plans():
     for quant in (1, 2, 3, 4):
         pl = frn.plan_launch(586, 7168, 8, quant, True, 152)
         assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 1 and pl["threads"] == 896
-        assert frn.plan_launch(1171, 7168, 8, quant, True, 152)["kernel"] == frn.KERNEL_STREAM
+        assert frn.plan_launch(1000, 7168, 8, quant, True, 152)["kernel"] == frn.KERNEL_STREAM
     assert frn.plan_launch(586, 7168, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
     assert frn.plan_launch(586, 7168, 4, 1, True, 152)["staged"] == 0
+    # many waves of wide rows: the row kernel again (with its prefetch one wave ahead)
+    for R, T in ((8, 1064), (8, 4682), (5, 1064), (4, 1520)):
+        pl = frn.plan_launch(T, 7168, R, 0, True, 152)
+        assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 0 and pl["threads"] == 896, (R, T)
+    assert frn.plan_launch(1063, 7168, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
+    assert frn.plan_launch(1519, 7168, 4, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
