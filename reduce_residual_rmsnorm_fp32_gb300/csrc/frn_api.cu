@@ -241,9 +241,10 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
 //  * a row for a wide CTA (H <= 8192, R <= 8): the row kernel below 2 rows per
 //    SM; beyond, the row kernel when two of its wide CTAs fit on an SM (R <= 2
 //    up to H = 8192, R <= 4 up to H = 5440, every output variant: e.g. 47 vs
-//    55 us at R = 4, T = 4096, H = 5120), else the stream kernel, whose overlap
-//    of one row's epilogue with the next rows' loads then wins (R = 3..4 at
-//    H = 7168: 68 vs 81 us at T = 4096);
+//    55 us at R = 4, T = 4096, H = 5120); else (one wide row per SM) the
+//    stream kernel, whose overlap of one row's epilogue with the next rows'
+//    loads then wins, up to the staged window and from many_waves on the row
+//    kernel with its prefetch one wave ahead;
 //  * a wider row: the stream kernel from one row per SM on, the row kernel's
 //    clusters with an FP8 output.
 int choose_kind(long long T, int H, int R, int quant, int num_sms) {
