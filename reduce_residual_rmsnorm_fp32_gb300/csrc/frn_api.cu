@@ -208,7 +208,7 @@ frn::RowPlan plan_rows(long long T, int H, int R, int quant, int num_sms) {
 // registers) when rows have few slices (R + 1 <= 4): there the consumers'
 // per-row epilogue, not HBM, sets the pace and more groups overlap more of it.
 // With more slices a deeper sub-ring per group pays more: 16 warps.
-frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
+frn::StreamPlan choose_stream(long long T, int H, int nslices, int quant, int num_sms) {
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
     const int tpw = ntiles <= 4 ? 1 : (ntiles <= 8 ? 2 : 4);
     frn::StreamPlan plan;
@@ -227,10 +227,17 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int num_sms) {
     while (groups > 1 && (groups * plan.consumer_warps + 1) > max_warps) --groups;
     plan.groups = groups;
     const int slice = 2 * H;
-    int slots = (frn::kStreamSmemLimit - frn::kStreamSmemReserve) / slice;
+    // Four tiles a warp re-read gamma every row; with a quant output the kernel
+    // keeps it in a shared-memory slice (the quant epilogue sets the pace).
+    // Measured on GB300: R = 8, T = 1000, H = 7168 FP8 B 32.4 -> 30.6 us;
+    // R = 2, T = 8192, H = 16384 MXFP4 A 198 -> 174 us; without quant the
+    // ring slot it takes cost 2-4 %.
+    plan.gamma_smem = tpw == 4 && quant != 0 ? 1 : 0;
+    const int gamma_bytes = plan.gamma_smem ? slice : 0;
+    int slots = (frn::kStreamSmemLimit - frn::kStreamSmemReserve - gamma_bytes) / slice;
     if (slots > frn::kStreamMaxSlots) slots = frn::kStreamMaxSlots;
     plan.slots = slots;
-    plan.smem_bytes = frn::stream_smem_bytes(slots, slice, groups);
+    plan.smem_bytes = frn::stream_smem_bytes(slots, slice, groups, gamma_bytes);
     plan.grid = T < num_sms ? T : num_sms;
     return plan;
 }
@@ -474,7 +481,7 @@ bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms)
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
     const frn::RowPlan rplan = plan_rows(c.T, c.H, c.R, quant, sms);
-    const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
+    const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), quant, sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
     unsigned int* status = nullptr;
@@ -569,7 +576,7 @@ frn_status run_unfused(Call c, int stages, frn_stream_t stream) {
     Call norm = c;
     norm.y = ytarget;
     const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
-    const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), sms);
+    const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), c.quant, sms);
     frn::Params p = make_params(norm, rplan, splan, nullptr);
     cudaError_t e = cudaSuccess;
     if (need_x) {
@@ -788,7 +795,7 @@ FRN_EXPORT frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int ha
     const int kind = choose_kind(T, H, R, quant, num_sms);
     out->kernel = kind;
     if (kind == kStream) {
-        const frn::StreamPlan plan = choose_stream(T, H, R + (has_residual ? 1 : 0), num_sms);
+        const frn::StreamPlan plan = choose_stream(T, H, R + (has_residual ? 1 : 0), quant, num_sms);
         out->ctas_per_row = 1;
         out->rows_per_cta = 1;
         out->tiles_per_warp = plan.tiles_per_warp;

@@ -44,9 +44,10 @@ constexpr int kStreamMaxSlots = 32;
 constexpr int kStreamSmemLimit = 232448;     // 227 KB opt-in per CTA on sm_100-class parts
 constexpr int kStreamSmemReserve = 3072;     // barriers, tile sums, flags (<= 16*32 + 4*512 + 16)
 
-__host__ __device__ constexpr int stream_smem_bytes(int slots, int slice_bytes, int groups) {
-    // data ring | full[slots], empty[slots] | tile sums [groups][2][kMaxTiles] | abort flag
-    return slots * slice_bytes + 16 * slots + groups * 2 * kMaxTiles * 4 + 16;
+// gamma_bytes: 2*H when gamma is kept in shared memory (four tiles a warp), else 0.
+__host__ __device__ constexpr int stream_smem_bytes(int slots, int slice_bytes, int groups, int gamma_bytes) {
+    // data ring | gamma | full[slots], empty[slots], gamma barrier (+pad) | tile sums [groups][2][kMaxTiles] | abort flag
+    return slots * slice_bytes + gamma_bytes + 16 * slots + 16 + groups * 2 * kMaxTiles * 4 + 16;
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting or
@@ -84,17 +85,26 @@ __device__ __forceinline__ bool consumers_sync_or(int id, bool pred, int nthread
 template <int TPW, int MODE, int MAXTHREADS>
 __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) unsigned char smem[];
+    // gamma stays in registers for 1-2 tiles a warp; with 4 it is re-read per
+    // row: with a quant output from a shared-memory slice (one bulk copy, so
+    // that the quant epilogue does not wait on L2 for it every row), without
+    // from cache (the slice would cost a ring slot, which measured slower).
+    constexpr bool kGammaInRegs = TPW < 4;
+    constexpr bool gamma_in_smem = !kGammaInRegs && (mode_fp8(MODE) || mode_mx(MODE));
     const int NC = p.consumer_warps;
     const int G = p.groups;
     const int S = p.slots;
     const int SG = S / G;              // slots of each group's sub-ring
     const uint32_t slice = static_cast<uint32_t>(p.slice_bytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slice);
-    float* tsum = reinterpret_cast<float*>(bars + 2 * S);
+    const uint32_t gamma_bytes = gamma_in_smem ? slice : 0u;
+    const uint4* gamma_s = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(S) * slice);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slice + gamma_bytes);
+    float* tsum = reinterpret_cast<float*>(bars + 2 * S + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tsum + G * 2 * kMaxTiles);
     const uint32_t data0 = smem_addr(smem);
     const uint32_t full0 = smem_addr(bars);
     const uint32_t empty0 = full0 + 8u * S;
+    const uint32_t gbar = full0 + 16u * S;   // counts the gamma copy
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -103,6 +113,7 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, static_cast<uint32_t>(NC));
         }
+        if (gamma_in_smem) mbar_init(gbar, 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -114,6 +125,10 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
     if (warp == G * NC) {
         // ------------------------------------------------------- producer --
         if (lane == 0) {
+            if (gamma_in_smem) {
+                mbar_arrive_expect_tx(gbar, slice);
+                bulk_g2s(smem_addr(gamma_s), p.gamma, slice, gbar);
+            }
             uint32_t issued = 0, issued_par = 0;
             int used[kStreamMaxGroups] = {0, 0, 0, 0};   // slices issued into each group's sub-ring
             bool ok = true;
@@ -151,6 +166,11 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
                     while (!mbar_try_wait(bar, par) && globaltimer_ns() - t0 <= p.wait_limit_ns) {
                     }
                 }
+                if (gamma_in_smem) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(gbar, 0u) && globaltimer_ns() - t0 <= p.wait_limit_ns) {
+                    }
+                }
             }
         }
         return;
@@ -159,9 +179,6 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
     // ----------------------------------------------------------- consumers --
     const int grp = warp / NC;
     const int lw = warp - grp * NC;            // warp index within the group
-    // gamma stays in registers for 1-2 tiles a warp; with 4 it is re-read from
-    // cache per row to keep the consumer inside its register budget.
-    constexpr bool kGammaInRegs = TPW < 4;
     int jt[TPW];
     bool vt[TPW];
     uint4 g[kGammaInRegs ? TPW : 1];
@@ -178,6 +195,7 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
     uint32_t ph = 0;
     int prow = 0;
     bool ok = true;
+    bool gamma_ready = !gamma_in_smem;   // the gamma copy has landed (waited for once)
     // this group's rows: the (grp + groups*m)-th rows of the CTA's sequence
     for (long long row = blockIdx.x + static_cast<long long>(grp) * gridDim.x; row < p.T;
          row += static_cast<long long>(G) * gridDim.x) {
@@ -216,13 +234,19 @@ __global__ void __launch_bounds__(MAXTHREADS, 1) frn_stream_kernel(const __grid_
             const float s = tile_sumsq(rov[t]);
             if (lane == 0 && lw + t * NC < p.ntiles) gsum[prow * kMaxTiles + lw + t * NC] = s;
         }
+        if (!gamma_ready) {
+            gamma_ready = true;
+            ok = ok && wait_bounded(gbar, 0u, abort_flag, p.wait_limit_ns, p.error_word);
+        }
         if (consumers_sync_or(1 + grp, !ok || *abort_flag != 0, NC * 32)) break;
         const float lo = lane < p.ntiles ? gsum[prow * kMaxTiles + lane] : 0.0f;
         const float hi = lane + 32 < p.ntiles ? gsum[prow * kMaxTiles + lane + 32] : 0.0f;
         const float rstd = row_rstd(lo, hi, p.H, p.eps);
 #pragma unroll
         for (int t = 0; t < TPW; ++t) {
-            const uint4 gt = kGammaInRegs ? g[kGammaInRegs ? t : 0] : ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
+            const uint4 gt = kGammaInRegs    ? g[kGammaInRegs ? t : 0]
+                           : gamma_in_smem ? (vt[t] ? gamma_s[jt[t]] : make_uint4(0u, 0u, 0u, 0u))
+                                           : ld_keep(p.gamma + (vt[t] ? jt[t] : 0), vt[t]);
             const uint4 yb = rms_y<false>(rov[t], rstd, gt);   // widened form: measured faster here
             if constexpr (mode_writes_y(MODE)) {
                 if (vt[t]) p.y[rbase + jt[t]] = yb;
@@ -254,6 +278,7 @@ struct StreamPlan {
     int consumer_warps;   // per group
     int groups;
     int slots;
+    int gamma_smem;       // four tiles a warp: gamma kept in a shared-memory slice
     int smem_bytes;
     long long grid;
 };
