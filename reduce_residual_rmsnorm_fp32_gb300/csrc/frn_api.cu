@@ -454,10 +454,13 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // The L2 prefetch pays when the grid is at most about two waves (most CTAs
 // start while the previous kernel on the stream drains, or while the first
 // wave runs) and there is enough to fetch: a single-CTA row of at least 32 KB
-// of loads, or a cluster CTA of at least 48 KB or a grid of at least 64
-// cluster CTAs.  Measured on GB300: below that, and for packed short rows
-// (up to 2x slower at H = 256), the extra requests cost more than the overlap
-// gives; beyond two waves it gains nothing.
+// of loads, or a cluster CTA of at least 48 KB or a grid of at least 32
+// cluster CTAs (with one request per input and CTA since the cluster CTAs
+// prefetch their slice whole: the decode step R = 8, H = 7168, T = 8, 16, 32,
+// 64 measured 9.54 -> 9.27 us per step with T = 8's 32 CTAs prefetching).
+// Measured on GB300: below that, and for packed short rows (up to 2x slower
+// at H = 256), the extra requests cost more than the overlap gives; beyond
+// two waves it gains nothing.
 // CTAs of a row-kernel launch resident on one SM: by threads (2048), CTAs
 // (32) and the registers the kernel's launch bound holds (row_min_blocks).
 long long row_ctas_per_sm(const frn::RowPlan& plan, int R) {
@@ -475,7 +478,7 @@ bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms)
     if (plan.grid * plan.threads > 2048LL * sms || plan.rows_per_cta > 1) return false;
     const long long row_bytes = 2LL * H * (R + 1);
     if (plan.ctas_per_row == 1) return row_bytes >= 32 * 1024;
-    return row_bytes / plan.ctas_per_row >= 48 * 1024 || T * plan.ctas_per_row >= 64;
+    return row_bytes / plan.ctas_per_row >= 48 * 1024 || T * plan.ctas_per_row >= 32;
 }
 
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
