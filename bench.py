@@ -690,9 +690,12 @@ PROFILE_CASES = {
     "decode64": (8, 64, H, "norm", False, 0.5),
     "decode8": (8, 8, H, "norm", False, 0.5),
     "decode16": (8, 16, H, "norm", False, 0.5),
+    "decode64_after_producer": (8, 64, H, "norm", False, 0.5),
+    "decode8_after_producer": (8, 8, H, "norm", False, 0.5),
     "staged_quant_a": (8, 586, H, "quant_a", False, 0.5),
     "sweep64M": (8, syn.sweep_tokens(64 << 20), H, "norm", False, 0.5),
     "sweep16M": (8, syn.sweep_tokens(16 << 20), H, "norm", False, 0.5),
+    "sweep8M": (8, syn.sweep_tokens(8 << 20), H, "norm", False, 0.5),
     "prefill_quant_a": (2, 8192, H, "quant_a", True, 1.0),
     "prefill_quant_b": (2, 8192, H, "quant_b", True, 1.0),
     "quant_R4_T32": (4, 32, 4096, "quant_b", False, 0.5),
@@ -702,7 +705,8 @@ PROFILE_CASES = {
 
 def run_profile_case(name: str, iters: int):
     """Launch one workload `iters` times (after 2 warm-up calls) and nothing else,
-    for ncu.  No timing is reported."""
+    for ncu; a case named ..._after_producer copies new values into the partials
+    right before each call.  No timing is reported."""
     import reduce_residual_rmsnorm_fp32_gb300 as frn
     R, T, Hh, mode, outlier, std = PROFILE_CASES[name]
     p, r, g = syn.make_inputs_device(R, T, Hh, seed=4242, partial_std=std, outlier_frac=0.01 if outlier else 0.0)
@@ -714,7 +718,10 @@ def run_profile_case(name: str, iters: int):
     else:
         q = torch.empty((T, Hh), dtype=torch.float8_e4m3fn, device="cuda") if mode != "norm" else None
         s = torch.empty((T, Hh // 128), dtype=torch.float32, device="cuda") if mode != "norm" else None
+    src = torch.randn(p.shape, device="cuda").to(torch.bfloat16) if name.endswith("_after_producer") else None
     for _ in range(2 + iters):
+        if src is not None:
+            p.copy_(src)      # the producer of the partials, right before the call
         if mode == "norm":
             frn.fused_reduce_rmsnorm(p, r, g, EPS, residual_out=ro, y=y)
         elif mode.startswith("mx"):
