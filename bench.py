@@ -692,7 +692,8 @@ PROFILE_CASES = {
     "decode16": (8, 16, H, "norm", False, 0.5),
     "decode64_after_producer": (8, 64, H, "norm", False, 0.5),
     "decode8_after_producer": (8, 8, H, "norm", False, 0.5),
-    "staged_quant_a": (8, 586, H, "quant_a", False, 0.5),
+    "staged_R16_T600_H4096": (16, 600, 4096, "norm", False, 0.5),
+    "stream_R8_T1024_H16384": (8, 1024, 16384, "norm", False, 0.5),
     "sweep64M": (8, syn.sweep_tokens(64 << 20), H, "norm", False, 0.5),
     "sweep16M": (8, syn.sweep_tokens(16 << 20), H, "norm", False, 0.5),
     "sweep8M": (8, syn.sweep_tokens(8 << 20), H, "norm", False, 0.5),

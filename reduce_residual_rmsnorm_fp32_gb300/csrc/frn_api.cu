@@ -110,12 +110,6 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
-// The row count from which wide rows with R >= 3 (one row per SM) take the row
-// kernel with its one-wave-ahead prefetch: seven waves for R >= 5 (R = 8,
-// H = 7168, T = 1171: no quant 31.9 vs 32.6 us, FP8 A 32.7 vs 34.1 us, FP8 B
-// 33.9 vs 36.1 us on the stream kernel), ten for R = 3, 4 (R = 4, T = 1171:
-// 22.1 vs 21.8 us; T = 2048: 34.8 vs 36.1 us).
-long long many_waves(int num_sms, int R) { return (R >= 5 ? 7LL : 10LL) * num_sms; }
 
 frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     const int nvec = H / frn::kVecElems;
@@ -176,27 +170,23 @@ frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
 }
 
 // Staged partial loads for a one-CTA row (two stages of two loads in flight,
-// 32 registers, so that two to four rows share an SM) where they measured
-// faster on GB300, each only once the grid is several waves of the
-// all-loads-at-once kernel (below that the second DRAM round trip of a row
-// shows: R = 16, H = 4096, T = 293: 10.6 vs 9.6 us):
-//  * R > 8 (rows of <= 16 tiles; 96 registers otherwise, one row per SM) from
-//    three waves: R = 16, H = 4096, T = 586 / 1171 / 4096: 16.8 / 29.7 / 95.8 us
-//    against 18.8 / 33.8 / 99.9 us;
-//  * R = 5..8 wide rows with a quant output at three to six waves, where they
-//    also beat the stream kernel: R = 8, H = 7168, T = 586: FP8 A 17.9 vs 19.5
-//    (stream 19.7) us, FP8 B 19.0 vs 21.0 (20.8), MXFP4 A 16.9 vs 18.8 (17.5);
-//    at T = 293 and from T = 1171 on they measured no better.
-bool staged_window(long long T, int H, int R, int quant, int num_sms) {
+// 32 registers, so that four 512-thread rows share an SM instead of one or
+// two) for R > 8 rows of <= 16 tiles (96 registers otherwise) from three
+// waves, where they measured faster on GB300: R = 16, H = 4096, T = 586 /
+// 1171 / 4096: 16.8 / 29.7 / 95.8 us against 18.8 / 33.8 / 99.9 us.  Below
+// three waves the second DRAM round trip of a row shows (T = 293: 10.6 vs
+// 9.6 us).  For R = 5..8 wide rows with a quant output they had beaten the
+// stream kernel at three to six waves (R = 8, H = 7168, T = 586: FP8 A 17.9
+// vs 19.7 us), but the all-loads-at-once row with its prefetch ahead now
+// beats both (17.5 us).
+bool staged_window(long long T, int H, int R, int num_sms) {
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
-    if (R > 8) return ntiles <= frn::kMaxTilesPerCta && T >= 3LL * num_sms;
-    return quant != 0 && R >= 5 && ntiles > frn::kMaxTilesPerCta && wide_possible(ntiles, R) &&
-           T >= 3LL * num_sms && T < 6LL * num_sms;
+    return R > 8 && ntiles <= frn::kMaxTilesPerCta && T >= 3LL * num_sms;
 }
 
-frn::RowPlan plan_rows(long long T, int H, int R, int quant, int num_sms) {
+frn::RowPlan plan_rows(long long T, int H, int R, int num_sms) {
     frn::RowPlan plan = choose_rows(T, H, R, num_sms);
-    if (plan.ctas_per_row == 1 && plan.rows_per_cta == 1 && staged_window(T, H, R, quant, num_sms))
+    if (plan.ctas_per_row == 1 && plan.rows_per_cta == 1 && staged_window(T, H, R, num_sms))
         plan.staged = 1;
     return plan;
 }
@@ -242,40 +232,22 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int quant, int nu
     return plan;
 }
 
-// Which kernel (measured on GB300 at H = 7168, R = 1..8, T = 8..8192):
-//  * a row that fits one 512-thread CTA (H <= 4096): the row kernel at any T
-//    (several rows in flight per SM);
-//  * a row for a wide CTA (H <= 8192, R <= 8): the row kernel below 2 rows per
-//    SM; beyond, the row kernel when two of its wide CTAs fit on an SM (R <= 2
-//    up to H = 8192, R <= 4 up to H = 5440, every output variant: e.g. 47 vs
-//    55 us at R = 4, T = 4096, H = 5120); else (one wide row per SM) the
-//    stream kernel, whose overlap of one row's epilogue with the next rows'
-//    loads then wins, up to the staged window and from many_waves on the row
-//    kernel with its prefetch one wave ahead;
+// Which kernel (measured on GB300 at H = 5120…8192, R = 1…8, T = 8…8192):
+//  * a row that fits one CTA (H <= 8192 with R <= 8, or H <= 4096): the row
+//    kernel at any T.  With one wide row per SM, its prefetch ahead and the
+//    first wave's own prefetch (launch_fused) keep HBM busy between rows, and
+//    it beats the stream kernel from two waves on in every output variant:
+//    R = 8, H = 7168, T = 586 no quant 16.6 vs 17.7 us, FP8 B 18.5 vs 19.4,
+//    MXFP4 B 17.8 vs 18.5; T = 880 23.5 vs 25.1 us; H = 8192, T = 586
+//    19.0 vs 21.1 us; H = 5120 13.5 vs 15.6 us; R = 4, H = 8192, T = 1171
+//    23.2 vs 24.0 us; R = 3, H = 7168, T = 1171 18.8 vs 19.7 us;
 //  * a wider row: the stream kernel from one row per SM on, the row kernel's
 //    clusters with an FP8 output.
 int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     const int forced = g_force_kernel.load(std::memory_order_relaxed);
     if (forced == kRows || forced == kStream) return forced;
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
-    if (ntiles <= frn::kMaxTilesPerCta) return kRows;
-    if (wide_possible(ntiles, R)) {
-        if (T < 2LL * num_sms) return kRows;
-        if (staged_window(T, H, R, quant, num_sms)) return kRows;
-        // From seven (R >= 5) or ten waves of one-per-SM rows on, the row
-        // kernel with its one-wave-ahead prefetch beats the stream kernel
-        // (R = 8, H = 7168: T = 2341 59.6 vs 62.5 us, T = 4682 109.8 vs
-        // 116.6 us; R = 4 / 5, T = 4096: 64.9 / 73.9 vs 68.4 / 78.5 us; FP8 A
-        // and MXFP4 B at T = 2341: 58.8 / 62.1 vs 60.2 / 65.2 us); below, the
-        // stream kernel.
-        if (T >= many_waves(num_sms, R)) return kRows;
-        // two or more wide rows resident per SM (threads, and the registers the
-        // launch bound holds: 32 for R <= 2, 48 for R <= 4, 64 for R <= 8)
-        const int threads = ntiles * 32;
-        const int regs = R <= 2 ? 32 : (R <= 4 ? 48 : 64);
-        const int by_threads = 2048 / threads, by_regs = 65536 / (threads * regs);
-        return (by_threads < by_regs ? by_threads : by_regs) >= 2 ? kRows : kStream;
-    }
+    if (ntiles <= frn::kMaxTilesPerCta || wide_possible(ntiles, R)) return kRows;
     // Wider rows: the stream kernel from one row per SM on -- except with an
     // FP8 output, where its single consumer group's quant epilogue, which
     // nothing overlaps, is slower than the row kernel's clusters (R = 2,
@@ -474,6 +446,24 @@ long long row_ctas_per_sm(const frn::RowPlan& plan, int R) {
     return n < by_regs ? n : by_regs;
 }
 
+// Distance of the prefetch ahead, in rows: about 9.5 MB of loads (R = 8,
+// H = 7168, one row per SM: 74 rows; R = 2, two rows per SM: 221), within a
+// quarter of a wave and one wave, in whole CTA spans.  Measured on GB300 at
+// H = 7168 against other fractions of a wave: R = 8 best at about half a wave
+// (T = 1171: 30.5 us at 0.5, 31.5 at 1, 31.2 at 0.25; T = 4682: 106.7 /
+// 108.4 / 109.4 us), R = 2 at 0.65-0.8 of a wave (T = 1024: 12.7 us at 0.65,
+// 13.3 at 1; T = 8192 FP8 A 81.9 / 82.1 us); two waves ahead was 5-14 % slower.
+long long ahead_rows(long long wave_rows, int rows_per_cta, int H, int nloads) {
+    constexpr long long kAheadBytes = 9728LL * 1024;
+    const long long row_bytes = 2LL * H * nloads;
+    long long n = (kAheadBytes + row_bytes / 2) / row_bytes;
+    const long long lo = wave_rows / 4 > 1 ? wave_rows / 4 : 1;
+    if (n < lo) n = lo;
+    if (n > wave_rows) n = wave_rows;
+    n -= n % rows_per_cta;
+    return n > 0 ? n : rows_per_cta;
+}
+
 bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms) {
     if (plan.grid * plan.threads > 2048LL * sms || plan.rows_per_cta > 1) return false;
     const long long row_bytes = 2LL * H * (R + 1);
@@ -483,7 +473,7 @@ bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms)
 
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
-    const frn::RowPlan rplan = plan_rows(c.T, c.H, c.R, quant, sms);
+    const frn::RowPlan rplan = plan_rows(c.T, c.H, c.R, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), quant, sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
@@ -499,21 +489,25 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // latency-bound: warp 0 alone computes rstd (measured -1..4% time at
     // T = 8192, H = 7168, R = 2; +2% at T = 32, where it is left off).
     p.rstd_one_warp = kind == kRows && rplan.grid * rplan.threads > 2048LL * sms;
-    // More rows than one wave holds, with R <= 2 (few loads in flight per SM):
-    // each CTA prefetches its span of the rows about one wave ahead (the CTAs
-    // resident an SM by threads and by the registers the launch bound holds),
-    // one bulk request per input.  Measured on GB300 at R = 2, H = 7168: +6%
-    // at T = 8192 without quant, +4..5% at T = 512..1024; at T = 8192 FP8 A
-    // 92.1 -> 81.9 us, MXFP4 A 86.0 -> 76.6 us (a request per warp and input
-    // instead measured -1% there).  With R >= 3 it pays only for wide rows
-    // (one row per SM) at many waves (many_waves; R = 8, H = 7168, T = 4682:
-    // 115.0 -> 109.8 us with the row kernel); at two waves it cost 10 %
-    // (R = 8, T = 293), and 4 % for 512-thread rows.
-    const bool wide_many = rplan.threads > frn::kMaxThreads && rplan.ctas_per_row == 1 && !rplan.staged &&
-                           c.T >= many_waves(sms, c.R);
-    if (kind == kRows && pf != 1 && (c.R <= 2 || wide_many)) {
-        const long long wave_rows = row_ctas_per_sm(rplan, c.R) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
-        if (wave_rows > 0 && c.T > wave_rows) p.prefetch_ahead = wave_rows;
+    // More rows than one wave holds, with R <= 2 (few loads in flight per SM)
+    // or, from 1.75 waves on, for wide rows: each CTA prefetches its span of
+    // the rows a fixed distance ahead (ahead_rows), one bulk request per
+    // input, and the first wave's CTAs their own span before the dependency
+    // wait.  Measured on GB300 at R = 2, H = 7168: +6% at T = 8192 without
+    // quant, +4..5% at T = 512..1024; at T = 8192 FP8 A 92.1 -> 81.9 us,
+    // MXFP4 A 86.0 -> 76.6 us (a request per warp and input instead measured
+    // -1% there).  Wide rows, R = 8, H = 7168: T = 4682 115.0 -> 106.7 us,
+    // T = 586 19.5 -> 16.6 us, T = 293 9.6 -> 9.4 us; below that it cost
+    // 2-4 % (T = 200, 250), and for 512-thread rows 4 %.  The first wave's
+    // own prefetch, which overlaps the previous kernel's tail: R = 8,
+    // T = 1171 31.7 -> 30.5 us, T = 2341 58.4 -> 57.2 us.
+    const long long wave_rows = row_ctas_per_sm(rplan, c.R) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
+    const bool wide = rplan.threads > frn::kMaxThreads && rplan.ctas_per_row == 1 && !rplan.staged;
+    if (kind == kRows && pf != 1 && (c.R <= 2 || (wide && 4 * c.T >= 7 * wave_rows))) {
+        if (wave_rows > 0 && c.T > wave_rows) {
+            p.prefetch_ahead = ahead_rows(wave_rows, rplan.rows_per_cta, c.H, c.R + (c.residual ? 1 : 0));
+            p.prefetch_own_below = wave_rows;
+        }
     }
     const bool pdl = g_pdl.load(std::memory_order_relaxed) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -809,7 +803,7 @@ FRN_EXPORT frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int ha
         out->threads = (plan.groups * plan.consumer_warps + 1) * 32;
         out->grid = plan.grid;
     } else {
-        const frn::RowPlan plan = plan_rows(T, H, R, quant, num_sms);
+        const frn::RowPlan plan = plan_rows(T, H, R, num_sms);
         out->ctas_per_row = plan.ctas_per_row;
         out->rows_per_cta = plan.rows_per_cta;
         out->tiles_per_warp = 1;

@@ -66,6 +66,8 @@ struct Params {
     int ntiles;              // ceil(nvec / 32)
     int prefetch_l2;         // row kernel: prefetch the row into L2 before the grid dependency wait
     long long prefetch_ahead;  // row kernel: also prefetch the row this many rows ahead (0: no)
+    long long prefetch_own_below;  // row kernel: CTAs whose first row is below this index (the first
+                                   // wave) also prefetch their own span before the dependency wait
     int rstd_one_warp;       // single-CTA row kernel: warp 0 alone computes rstd and shares it
     int tiles_per_cta;       // warps per row in a CTA (row kernel)
     int rows_per_cta;        // single-CTA row kernel: consecutive rows per CTA

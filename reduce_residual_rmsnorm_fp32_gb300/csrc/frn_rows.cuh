@@ -84,11 +84,11 @@ constexpr int row_min_blocks(int rmax, bool cluster, int maxt, bool staged = fal
                                   : (rmax <= 2 ? 4 : rmax <= 4 ? 3 : rmax <= 8 ? 2 : 1);
 }
 
-// STAGED (single-CTA rows, RMAX 8 or 16): a thread keeps two stages of two
-// partial loads in flight instead of all R at once, and sums them in rank
-// order as they arrive, so that it fits 32 registers -- two rows of up to 8192
-// elements resident per SM instead of one, which keeps loads in flight while
-// the other row runs its epilogue.
+// STAGED (single-CTA rows of at most kMaxThreads, R > 8): a thread keeps two
+// stages of two partial loads in flight instead of all R at once, and sums
+// them in rank order as they arrive, so that it fits 32 registers -- four
+// 512-thread rows resident per SM instead of one, which keeps loads in flight
+// while the other rows run their epilogues.
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads, bool STAGED = false>
 __global__ void __launch_bounds__(MAXT, row_min_blocks(RMAX, CLUSTER, MAXT, STAGED))
 frn_row_kernel(const __grid_constant__ Params p) {
@@ -147,10 +147,17 @@ frn_row_kernel(const __grid_constant__ Params p) {
             if (tile < p.ntiles && in_rows) prefetch_tile_span(p, row, tile, lane, true);
         }
     }
-    // Many rows: ask for this CTA's span of the rows about one wave of CTAs
-    // ahead, so that the CTA which takes them finds them in L2.
+    // Many rows: ask for this CTA's span of the rows a fixed distance ahead,
+    // so that the CTA which takes them finds them in L2; the first wave's
+    // CTAs, which start while the previous kernel drains, first ask for their
+    // own span.
     if (p.prefetch_ahead > 0 && warp == 0) {
         const long long row0 = kPacked ? static_cast<long long>(blockIdx.x) * p.rows_per_cta : row;
+        if (row0 < p.prefetch_own_below) {
+            const long long left = p.T - row0;
+            const int nrows = kPacked ? static_cast<int>(left < p.rows_per_cta ? left : p.rows_per_cta) : 1;
+            prefetch_cta_span(p, row0, nrows, rank * p.tiles_per_cta, lane, true);
+        }
         const long long ahead = row0 + p.prefetch_ahead;
         if (ahead < p.T) {
             const long long left = p.T - ahead;
@@ -321,7 +328,7 @@ struct RowPlan {
     int rows_per_cta;   // single-CTA rows only: short rows share a CTA
     int threads;
     long long grid;
-    int staged;         // single-CTA rows with R >= 3: staged partial loads (STAGED)
+    int staged;         // single-CTA rows with R > 8: staged partial loads (STAGED)
 };
 
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads, bool STAGED = false>
@@ -368,12 +375,9 @@ cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t st
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
-    if (plan.staged) {
-        // one CTA per row, R >= 3 (R <= 8 for a wide CTA)
-        if (plan.threads > kMaxThreads) return launch_row_one<8, MODE, false, 1024, true>(p, plan, stream, pdl);
-        if (p.R <= 8) return launch_row_one<8, MODE, false, kMaxThreads, true>(p, plan, stream, pdl);
-        return launch_row_one<16, MODE, false, kMaxThreads, true>(p, plan, stream, pdl);
-    }
+    // staged loads: one CTA of at most kMaxThreads per row, R > 8 (the host
+    // plans nothing else)
+    if (plan.staged) return launch_row_one<16, MODE, false, kMaxThreads, true>(p, plan, stream, pdl);
     if (plan.threads > kMaxThreads) {
         // one wide CTA per row (the host only plans this for R <= 8)
         if (p.R <= 1) return launch_row_one<1, MODE, false, 1024>(p, plan, stream, pdl);

@@ -25,8 +25,8 @@ def lib():
 def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
     ntiles = -(-(H // 8) // 32)
     what = (T, H, R, quant, residual, sms, pl)
-    if auto and ntiles <= 16:
-        assert pl["kernel"] == frn.KERNEL_ROWS, what
+    if auto and (ntiles <= 16 or (ntiles <= 32 and R <= 8)):
+        assert pl["kernel"] == frn.KERNEL_ROWS, what                    # every row that fits one CTA
     if pl["kernel"] == frn.KERNEL_ROWS:
         C, tpc, rows, thr = pl["ctas_per_row"], pl["tiles_per_cta"], pl["rows_per_cta"], pl["threads"]
         assert 1 <= C <= 16 and tpc >= 1 and rows >= 1, what
@@ -42,8 +42,7 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
         assert pl["grid"] == -(-T // rows) * C, what
         assert pl["smem_bytes"] == 0, what
         if pl["staged"]:                                                   # staged loads: one CTA a row
-            assert C == 1 and rows == 1 and R >= 5 and T >= 3 * sms, what
-            assert (R > 8 and ntiles <= 16) or (quant and thr > 512 and T < 6 * sms), what
+            assert C == 1 and rows == 1 and R > 8 and ntiles <= 16 and T >= 3 * sms, what
     else:
         tpw, nc, g, slots = pl["tiles_per_warp"], pl["consumer_warps"], pl["groups"], pl["slots"]
         nslices = R + (1 if residual else 0)
@@ -131,20 +130,17 @@ def test_query_launch_checks_sizes_then_needs_a_device():
 
 def test_staged_plans():
     """Staged partial loads where they measured faster: R > 8 rows of up to 16
-    tiles from three waves; R = 5..8 wide rows with a quant output at three to
-    six waves (there the row kernel, not the stream kernel)."""
+    tiles from three waves.  Wide rows (17-32 tiles, R <= 8) take the row
+    kernel with every output at every T, loading all partials at once."""
     pl = frn.plan_launch(600, 4096, 16, 0, True, 152)
     assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 1 and pl["threads"] == 512
     assert frn.plan_launch(300, 4096, 16, 0, True, 152)["staged"] == 0
-    for quant in (1, 2, 3, 4):
-        pl = frn.plan_launch(586, 7168, 8, quant, True, 152)
-        assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 1 and pl["threads"] == 896
-        assert frn.plan_launch(1000, 7168, 8, quant, True, 152)["kernel"] == frn.KERNEL_STREAM
-    assert frn.plan_launch(586, 7168, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
-    assert frn.plan_launch(586, 7168, 4, 1, True, 152)["staged"] == 0
-    # many waves of wide rows: the row kernel again (with its prefetch one wave ahead)
-    for R, T in ((8, 1064), (8, 4682), (5, 1064), (4, 1520)):
-        pl = frn.plan_launch(T, 7168, R, 0, True, 152)
-        assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 0 and pl["threads"] == 896, (R, T)
-    assert frn.plan_launch(1063, 7168, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
-    assert frn.plan_launch(1519, 7168, 4, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
+    for quant in (0, 1, 2, 3, 4):
+        for R, T in ((8, 586), (8, 1000), (5, 586), (4, 1519), (8, 1063), (8, 4682), (3, 1171)):
+            pl = frn.plan_launch(T, 7168, R, quant, True, 152)
+            assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 0 and pl["threads"] == 896, (R, T, quant)
+    # rows wider than one CTA: the stream kernel from one row per SM (not with FP8)
+    assert frn.plan_launch(1000, 16384, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
+    assert frn.plan_launch(1000, 16384, 8, 3, True, 152)["kernel"] == frn.KERNEL_STREAM
+    assert frn.plan_launch(1000, 16384, 8, 1, True, 152)["kernel"] == frn.KERNEL_ROWS
+    assert frn.plan_launch(1000, 8192, 16, 0, True, 152)["kernel"] == frn.KERNEL_STREAM

@@ -356,7 +356,7 @@ def test_stream_consumer_groups(groups, R, T, H):
         frn.set_kernel(frn.KERNEL_AUTO)
 
 
-@pytest.mark.parametrize("R,T,H", [(16, 600, 4096), (9, 500, 2048), (8, 586, 7168), (5, 500, 7168), (7, 470, 7936),
+@pytest.mark.parametrize("R,T,H", [(16, 600, 4096), (9, 500, 2048), (10, 1000, 4096), (16, 457, 3968),
                                    (12, 460, 1024)])
 def test_staged_loads(R, T, H):
     """Rows whose partials are loaded in stages (two stages of two in flight),
