@@ -447,7 +447,7 @@ long long row_ctas_per_sm(const frn::RowPlan& plan, int R) {
 }
 
 // Distance of the prefetch ahead, in rows: about 9.5 MB of loads (R = 8,
-// H = 7168, one row per SM: 74 rows; R = 2, two rows per SM: 221), within a
+// H = 7168, one row per SM: 77 rows; R = 2, two rows per SM: 232), within a
 // quarter of a wave and one wave, in whole CTA spans.  Measured on GB300 at
 // H = 7168 against other fractions of a wave: R = 8 best at about half a wave
 // (T = 1171: 30.5 us at 0.5, 31.5 at 1, 31.2 at 0.25; T = 4682: 106.7 /
@@ -466,6 +466,12 @@ long long ahead_rows(long long wave_rows, int rows_per_cta, int H, int nloads) {
 
 bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms) {
     if (plan.grid * plan.threads > 2048LL * sms || plan.rows_per_cta > 1) return false;
+    // Wide rows: only when the registers hold the whole grid at once too (one
+    // or two rows an SM); beyond, the prefetch ahead takes over (R = 8,
+    // H = 7168: T = 250 8.5 -> 8.0 us, T = 293 9.65 -> 9.1 us, T = 347
+    // 12.3 -> 11.55 us).
+    if (plan.threads > frn::kMaxThreads && plan.ctas_per_row == 1 && plan.grid > row_ctas_per_sm(plan, R) * sms)
+        return false;
     const long long row_bytes = 2LL * H * (R + 1);
     if (plan.ctas_per_row == 1) return row_bytes >= 32 * 1024;
     return row_bytes / plan.ctas_per_row >= 48 * 1024 || T * plan.ctas_per_row >= 32;
@@ -490,20 +496,19 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // T = 8192, H = 7168, R = 2; +2% at T = 32, where it is left off).
     p.rstd_one_warp = kind == kRows && rplan.grid * rplan.threads > 2048LL * sms;
     // More rows than one wave holds, with R <= 2 (few loads in flight per SM)
-    // or, from 1.75 waves on, for wide rows: each CTA prefetches its span of
-    // the rows a fixed distance ahead (ahead_rows), one bulk request per
-    // input, and the first wave's CTAs their own span before the dependency
-    // wait.  Measured on GB300 at R = 2, H = 7168: +6% at T = 8192 without
-    // quant, +4..5% at T = 512..1024; at T = 8192 FP8 A 92.1 -> 81.9 us,
-    // MXFP4 A 86.0 -> 76.6 us (a request per warp and input instead measured
-    // -1% there).  Wide rows, R = 8, H = 7168: T = 4682 115.0 -> 106.7 us,
-    // T = 586 19.5 -> 16.6 us, T = 293 9.6 -> 9.4 us; below that it cost
-    // 2-4 % (T = 200, 250), and for 512-thread rows 4 %.  The first wave's
-    // own prefetch, which overlaps the previous kernel's tail: R = 8,
+    // or for wide rows: each CTA prefetches its span of the rows a fixed
+    // distance ahead (ahead_rows), one bulk request per input, and the first
+    // wave's CTAs their own span before the dependency wait.  Measured on
+    // GB300 at R = 2, H = 7168: +6% at T = 8192 without quant, +4..5% at
+    // T = 512..1024; at T = 8192 FP8 A 92.1 -> 81.9 us, MXFP4 A 86.0 -> 76.6 us
+    // (a request per warp and input instead measured -1% there).  Wide rows,
+    // R = 8, H = 7168: T = 4682 115.0 -> 106.7 us, T = 586 19.5 -> 16.6 us,
+    // T = 170 7.2 -> 7.0 us; for 512-thread rows it cost 4 %.  The first
+    // wave's own prefetch, which overlaps the previous kernel's tail: R = 8,
     // T = 1171 31.7 -> 30.5 us, T = 2341 58.4 -> 57.2 us.
     const long long wave_rows = row_ctas_per_sm(rplan, c.R) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
     const bool wide = rplan.threads > frn::kMaxThreads && rplan.ctas_per_row == 1 && !rplan.staged;
-    if (kind == kRows && pf != 1 && (c.R <= 2 || (wide && 4 * c.T >= 7 * wave_rows))) {
+    if (kind == kRows && pf != 1 && (c.R <= 2 || wide)) {
         if (wave_rows > 0 && c.T > wave_rows) {
             p.prefetch_ahead = ahead_rows(wave_rows, rplan.rows_per_cta, c.H, c.R + (c.residual ? 1 : 0));
             p.prefetch_own_below = wave_rows;

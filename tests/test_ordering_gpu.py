@@ -52,10 +52,12 @@ def test_same_stream_slow_producer(pdl):
     assert_y_close(host_bits(y), ry)
 
 
-@pytest.mark.parametrize("shape", [(4, 16, 4096), (8, 16, 7168), (8, 64, 7168), (2, 700, 256)],
-                         ids=["single_cta", "cluster", "wide", "packed"])
+@pytest.mark.parametrize("shape", [(4, 16, 4096), (8, 16, 7168), (8, 64, 7168), (2, 700, 256), (8, 586, 7168),
+                                   (2, 700, 7168)],
+                         ids=["single_cta", "cluster", "wide", "packed", "wide_waves", "r2_waves"])
 def test_slow_producer_with_l2_prefetch_forced_on(shape):
-    """The kernels prefetch their rows into L2 before the dependency wait.  With
+    """The kernels prefetch their rows into L2 before the dependency wait (and,
+    over several waves, the first wave's rows and rows further ahead).  With
     the prefetch forced on for every row-kernel shape and a slow producer that
     overwrites the partials (zeros before) only after ~10 ms, the prefetched
     lines hold the old zeros, yet every value the kernel reads after the wait is
