@@ -307,9 +307,10 @@ int frn_version(void);
  * frn_set_l2_prefetch: row kernel only.  0 (default) decides from the launch
  *   shape whether each warp asks for its slice of the row to be fetched into
  *   L2 before the wait on the previous kernel, and, for grids of more than
- *   one wave, for the same slice of the row one wave ahead (hints that hand
- *   no value to the kernel); 1 does neither; 2 always does the first and
- *   decides the second as 0 does.
+ *   one wave, whether each CTA asks for its slice of the row about 9.5 MB of
+ *   loads ahead (and the first wave's CTAs for their own, before the wait):
+ *   hints that hand no value to the kernel; 1 does neither; 2 always does the
+ *   first and decides the second as 0 does.
  */
 frn_status frn_set_pdl(int enable);
 frn_status frn_set_l2_prefetch(int mode);
