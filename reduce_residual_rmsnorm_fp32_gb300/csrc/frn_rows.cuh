@@ -216,17 +216,16 @@ frn_row_kernel(const __grid_constant__ Params p) {
 
     const float s = tile_sumsq(ro);
 
-    // x * gamma needs no rstd: the single-CTA shapes form it before the row
-    // barrier, and store residual_out there too, so that this runs while the
-    // other warps catch up -- except with a quant output in the 512-thread
-    // shape (the early store measured slower at the FP8 decode workload) and
-    // the packed 256-thread shape (both, tight on registers).  A cluster forms
-    // it while the tile sums travel; every global store of its threads comes
-    // after the cluster synchronisation, so that no barrier operation waits
-    // for outstanding stores.
+    // x * gamma and residual_out need no rstd: they are formed and stored
+    // before the row barrier (a cluster's while its tile sums travel), so
+    // that this runs while the other warps or CTAs catch up -- except with a
+    // quant output in the 512-thread shapes (the early store measured slower
+    // at the FP8 decode workload) and the packed 256-thread shape (both, tight
+    // on registers).  In a cluster the early store measured 4-9 % faster at
+    // decode T = 8…32 (R = 8, H = 7168) than storing after the exchange.
     constexpr bool kQuantOut = mode_fp8(MODE) || mode_mx(MODE);
     constexpr bool kEarlyXg = CLUSTER || !(MAXT == kPackedThreads && kQuantOut);
-    constexpr bool kEarlyStore = !CLUSTER && kEarlyXg && !(MAXT == kMaxThreads && kQuantOut);
+    constexpr bool kEarlyStore = kEarlyXg && !(MAXT == kMaxThreads && kQuantOut);
     float xg[8];
     // The FP8 group's absmax of y follows from the absmax of x * gamma (see
     // xgamma_group_absmax), so its shuffles can run before rstd is known too
@@ -237,6 +236,9 @@ frn_row_kernel(const __grid_constant__ Params p) {
         else return 0.0f;
     };
     float lo, hi;   // tile slots `lane` and `lane + 32` of the row
+    if constexpr (kEarlyStore) {
+        if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
+    }
     if constexpr (CLUSTER) {
         cluster_wait_acquire();   // every CTA of the cluster has armed its row barrier
         // (test hook: tile 0's sum is never pushed, so every CTA's wait runs out)
@@ -250,9 +252,6 @@ frn_row_kernel(const __grid_constant__ Params p) {
         lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
         hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
     } else {
-        if constexpr (kEarlyStore) {
-            if (valid && p.residual_out != nullptr) p.residual_out[off] = ro;
-        }
         if constexpr (kEarlyXg) {
             xgamma8(ro, g, xg);
             amax_xg = quant_lanes_absmax(xg);
