@@ -190,6 +190,37 @@ def test_many_row_launches_are_bit_identical(R):
         assert np.array_equal(np.asarray(a)[:13].view(np.uint8), np.asarray(c).view(np.uint8))
 
 
+@pytest.mark.parametrize("R,T,H,with_residual", [
+    (8, 153, 7168, True),     # one row past a wave of wide rows
+    (8, 400, 7000, True),     # ragged last tile
+    (1, 1000, 7168, True),    # two wide rows an SM
+    (3, 800, 5120, True),     # two 640-thread rows an SM
+    (2, 5000, 256, True),     # packed short rows, eight to a CTA
+    (2, 700, 7168, False),    # no residual: R loads a row
+    (8, 1171, 7168, False),
+])
+def test_prefetch_ahead_paths(R, T, H, with_residual):
+    """Grids of more than one wave, where each CTA prefetches the rows a fixed
+    distance ahead and the first wave its own rows before the dependency wait:
+    every row against the oracle, and the same bits with every prefetch off."""
+    inp = syn.make_inputs(R, T, H, seed=90 + R + T + H, partial_std=0.5, with_residual=with_residual)
+    assert frn.query_launch(T, H, R, 0, with_residual)[0] == frn.KERNEL_ROWS
+    quant = H % 128 == 0 and with_residual
+    if quant:
+        check_quant(inp, f"ahead R={R} T={T} H={H}")
+    else:
+        check_norm(inp, f"ahead R={R} T={T} H={H} res={with_residual}")
+    d = DevInputs(inp)
+    base = gpu_quant(d, True) if quant else gpu_norm(d)
+    frn.set_l2_prefetch(1)
+    try:
+        off = gpu_quant(d, True) if quant else gpu_norm(d)
+    finally:
+        frn.set_l2_prefetch(0)
+    for a, b in zip(base, off):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
 @pytest.mark.parametrize("H", [256, 512, 768, 1024])
 @pytest.mark.parametrize("R", [1, 2, 8])
 def test_packed_short_rows(H, R):
