@@ -755,6 +755,8 @@ def main():
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -766,64 +768,55 @@ def main():
     torch.cuda.set_device(dev)
     hbm, peak_kind = peaks()
 
-    # ---- headline: decode steps over rotating input sets, as graph replays.
-    # One graph holds one step per input set, in order (as a decode graph holds
-    # the epilogues of all its layers); one graph of exactly that many steps
-    # runs the remainder when the step count is not a multiple of the set count.
+    # ---- headline: decode steps over rotating input sets, as graph replays
+    # (a decode graph holds the epilogues of all its layers).
     per_set = sum(syn.algorithmic_bytes(R_DEC, T, H, "norm") for T in DECODE_T)
     nsets = max(16, sets_to_beat_l2(per_set))
     gamma = syn.make_inputs_device(1, 1, H, seed=3)[2]
     sets = [DecodeSet(seed=rank * 10000 + k, gamma=gamma) for k in range(nsets)]
 
-    def all_sets():
-        for st in sets:
-            st.step(frn)
-    chain = capture(all_sets)
-    # The timed region is one graph launch of exactly K steps (the sets in
-    # rotation) when K is at most ONE_GRAPH_MAX; beyond that, K // nsets
-    # replays of the chain and one graph of the remaining steps, whose single
-    # switch between graphs is then spread over more than ONE_GRAPH_MAX steps.
-    # Every graph is launched once before the timed region (a first launch
-    # uploads it), and the launch right before the start event is of the same
-    # graph as the timed one.
+    # The timed region replays only graphs captured for it: one graph of
+    # exactly K steps (the sets in rotation) when K is at most ONE_GRAPH_MAX;
+    # beyond that, K // nsets replays of a one-pass graph (one step per set)
+    # and one graph of the remaining steps.  Nothing else is captured before
+    # the timed region, and the warm-up replays the timed graphs themselves:
+    # measured on GB300, once a process has captured further graphs, replays
+    # of these kernels run about 6 % slower whichever graph is timed (a
+    # 16-step graph replayed back to back: 8.84 us a step alone, 9.43 us
+    # after one more 20-step graph was captured; deleting that graph did not
+    # bring it back).  Every graph is launched once before the timed region (a
+    # first launch uploads it).
     ONE_GRAPH_MAX = 2048
-    tails = {}
 
-    def tail(k):
-        """A graph of k steps, the sets in rotation, captured ahead of the timed region."""
-        if k not in tails:
-            tails[k] = capture(lambda: [sets[i % nsets].step(frn) for i in range(k)])
-        return tails[k]
+    def steps_graph(k):
+        return capture(lambda: [sets[i % nsets].step(frn) for i in range(k)])
 
-    def plan(n):
-        if n <= ONE_GRAPH_MAX:
-            return [(tail(n), 1)] if n else []
-        parts = [(chain, n // nsets)]
-        if n % nsets:
-            parts.append((tail(n % nsets), 1))
-        return parts
+    if args.steps <= ONE_GRAPH_MAX:
+        timed = [(steps_graph(args.steps), 1)]
+    else:
+        timed = [(steps_graph(nsets), args.steps // nsets)]
+        if args.steps % nsets:
+            timed.append((steps_graph(args.steps % nsets), 1))
 
-    for g, _ in plan(args.steps) + plan(args.warmup):
-        g.replay()
-    torch.cuda.synchronize()
-
-    def run_steps(n):
-        for g, reps in plan(n):
+    def run_timed():
+        for g, reps in timed:
             for _ in range(reps):
                 g.replay()
 
-    # clocks are sampled from here to the end of the timed region: a ~0.5 s
-    # stretch of the same steps first (part of the warm-up), then the timed steps
+    for g, _ in timed:
+        g.replay()
+    torch.cuda.synchronize()
+
+    # clocks are sampled from here to the end of the timed region: at least W
+    # steps and about 0.5 s of the timed graphs first, then the timed steps
     sampler = ClockSampler(local)
     sampler.start()
-    # (the timed region's own graphs replayed over and over: a graph's first
-    # few launches run slower than later ones)
     t_end = time.perf_counter() + 0.5
-    run_steps(args.warmup)
-    reps = 0
-    while time.perf_counter() < t_end or reps < 3:
-        run_steps(max(args.steps, nsets))
+    warm_steps = reps = 0
+    while time.perf_counter() < t_end or warm_steps < args.warmup or reps < 3:
+        run_timed()
         torch.cuda.synchronize()
+        warm_steps += args.steps
         reps += 1
     torch.cuda.synchronize()
     barrier(world)
@@ -833,11 +826,9 @@ def main():
     # before the start event: the GPU runs it while the host enqueues the timed
     # graphs, so the events bracket the device time of exactly the K timed
     # steps, not the host's latency to submit the first graph to an idle GPU.
-    timed = plan(args.steps)
-    if timed:
-        timed[0][0].replay()
+    timed[0][0].replay()
     e0.record()
-    run_steps(args.steps)
+    run_timed()
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -845,7 +836,7 @@ def main():
     elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     bytes_per_step = step_bytes()
     value = world * bytes_per_step * args.steps / elapsed / 1e9
-    del chain, tails, sets
+    del timed, sets
     torch.cuda.empty_cache()
 
     extras = {}
