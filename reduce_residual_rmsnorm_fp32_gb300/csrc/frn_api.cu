@@ -105,19 +105,43 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
     plan.threads = ntiles * 32;
     plan.grid = T;
     plan.staged = 0;
+    plan.tiles_per_warp = 1;
     return plan;
 }
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
+// Rows of 33..64 tiles (8192 < H <= 16384) with R <= 2 from two waves on: one
+// CTA per row, two tiles a warp (frn_row2_kernel), instead of a cluster of
+// CTAs or the stream kernel -- except MXFP4 without y, where the stream
+// kernel (gamma in shared memory) stays ahead.  Measured on GB300 at R = 2,
+// T = 8192, H = 16384 (two-tile row / stream / clusters of 4, us): no quant
+// 192.7 / 201.2 / 244.4, FP8 A 182.3 / 287.1 / 269.5, FP8 B 213.3 / 280.4 /
+// 284.6, MXFP4 B 203.0 / 246.8 / 281.6, MXFP4 A 175.9 / 167.2 / 259.2; H =
+// 12288 FP8 A 152.9 / 173.9 / 200.7; R = 1, H = 16384 FP8 A 163.8 / 270.0 /
+// 256.0; R = 2, H = 16384, T = 600 FP8 A 18.4 / 29.5 / 23.1.
+bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
+    return ntiles > 2 * frn::kMaxTilesPerCta && R <= 2 && quant != 3 && T >= 2LL * num_sms;
+}
 
-frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
+frn::RowPlan two_tile_plan(long long T, int ntiles) {
+    frn::RowPlan plan = wide_plan(T, ntiles);
+    plan.threads = ceil_div(ntiles, 2) * 32;
+    plan.tiles_per_warp = 2;
+    return plan;
+}
+
+
+frn::RowPlan choose_rows(long long T, int H, int R, int quant, int num_sms) {
     const int nvec = H / frn::kVecElems;
     const int ntiles = ceil_div(nvec, frn::kTileVecs);
     const int cmin = ceil_div(ntiles, frn::kMaxTilesPerCta);
     int C;
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
     if (forced == 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
+    if ((forced == 1 && ntiles > 2 * frn::kMaxTilesPerCta && R <= 2) ||
+        (forced == 0 && two_tile_rows(T, ntiles, R, quant, num_sms)))
+        return two_tile_plan(T, ntiles);
     if (forced > 0) {
         // up to 8 CTAs per cluster with at least one tile each; up to 16
         // (non-portable cluster size) with at least two tiles each
@@ -166,6 +190,7 @@ frn::RowPlan choose_rows(long long T, int H, int R, int num_sms) {
     plan.threads = plan.rows_per_cta * tpc * 32;
     plan.grid = (T + plan.rows_per_cta - 1) / plan.rows_per_cta * C;
     plan.staged = 0;
+    plan.tiles_per_warp = 1;
     return plan;
 }
 
@@ -184,8 +209,8 @@ bool staged_window(long long T, int H, int R, int num_sms) {
     return R > 8 && ntiles <= frn::kMaxTilesPerCta && T >= 3LL * num_sms;
 }
 
-frn::RowPlan plan_rows(long long T, int H, int R, int num_sms) {
-    frn::RowPlan plan = choose_rows(T, H, R, num_sms);
+frn::RowPlan plan_rows(long long T, int H, int R, int quant, int num_sms) {
+    frn::RowPlan plan = choose_rows(T, H, R, quant, num_sms);
     if (plan.ctas_per_row == 1 && plan.rows_per_cta == 1 && staged_window(T, H, R, num_sms))
         plan.staged = 1;
     return plan;
@@ -248,6 +273,7 @@ int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     if (forced == kRows || forced == kStream) return forced;
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
     if (ntiles <= frn::kMaxTilesPerCta || wide_possible(ntiles, R)) return kRows;
+    if (two_tile_rows(T, ntiles, R, quant, num_sms)) return kRows;
     // Wider rows: the stream kernel from one row per SM on -- except with an
     // FP8 output, where its single consumer group's quant epilogue, which
     // nothing overlaps, is slower than the row kernel's clusters (R = 2,
@@ -436,6 +462,7 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // CTAs of a row-kernel launch resident on one SM: by threads (2048), CTAs
 // (32) and the registers the kernel's launch bound holds (row_min_blocks).
 long long row_ctas_per_sm(const frn::RowPlan& plan, int R) {
+    if (plan.tiles_per_warp == 2) return 1;   // frn_row2_kernel: launch bound (1024, 1), up to 1024 threads
     const bool cluster = plan.ctas_per_row > 1;
     const int maxt = plan.rows_per_cta > 1 ? frn::kPackedThreads : (plan.threads > frn::kMaxThreads ? 1024 : frn::kMaxThreads);
     const int rmax = R <= 1 ? 1 : R <= 2 ? 2 : R <= 4 ? 4 : R <= 8 ? 8 : 16;
@@ -479,7 +506,7 @@ bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms)
 
 frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) {
     const int kind = choose_kind(c.T, c.H, c.R, quant, sms);
-    const frn::RowPlan rplan = plan_rows(c.T, c.H, c.R, sms);
+    const frn::RowPlan rplan = plan_rows(c.T, c.H, c.R, quant, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), quant, sms);
     if (kind == kRows && rplan.grid > 0x7FFFFFFFLL)
         return fail(FRN_ERR_UNSUPPORTED, "grid too large (T=%lld)", static_cast<long long>(c.T));
@@ -503,12 +530,16 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // T = 512..1024; at T = 8192 FP8 A 92.1 -> 81.9 us, MXFP4 A 86.0 -> 76.6 us
     // (a request per warp and input instead measured -1% there).  Wide rows,
     // R = 8, H = 7168: T = 4682 115.0 -> 106.7 us, T = 586 19.5 -> 16.6 us,
-    // T = 170 7.2 -> 7.0 us; for 512-thread rows it cost 4 %.  The first
-    // wave's own prefetch, which overlaps the previous kernel's tail: R = 8,
-    // T = 1171 31.7 -> 30.5 us, T = 2341 58.4 -> 57.2 us.
+    // T = 170 7.2 -> 7.0 us; for 512-thread rows it cost 4 %.  Cluster rows
+    // with R > 2 from two waves on: R = 8, T = 2048, H = 16384 FP8 A 134.8 ->
+    // 123.9 us, FP8 B 144.4 -> 137.8 us; R = 4, T = 4096 FP8 B 221.6 ->
+    // 207.3 us (at T = 64 it cost 3 %).  The first wave's own prefetch, which
+    // overlaps the previous kernel's tail: R = 8, T = 1171 31.7 -> 30.5 us,
+    // T = 2341 58.4 -> 57.2 us.
     const long long wave_rows = row_ctas_per_sm(rplan, c.R) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
     const bool wide = rplan.threads > frn::kMaxThreads && rplan.ctas_per_row == 1 && !rplan.staged;
-    if (kind == kRows && pf != 1 && (c.R <= 2 || wide)) {
+    const bool cluster_waves = rplan.ctas_per_row > 1 && c.T >= 2 * wave_rows;
+    if (kind == kRows && pf != 1 && (c.R <= 2 || wide || cluster_waves)) {
         if (wave_rows > 0 && c.T > wave_rows) {
             p.prefetch_ahead = ahead_rows(wave_rows, rplan.rows_per_cta, c.H, c.R + (c.residual ? 1 : 0));
             p.prefetch_own_below = wave_rows;
@@ -577,7 +608,7 @@ frn_status run_unfused(Call c, int stages, frn_stream_t stream) {
                          : reinterpret_cast<uint4*>(ws + (need_x ? 4LL * c.T * c.H : 0));
     Call norm = c;
     norm.y = ytarget;
-    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, sms);
+    const frn::RowPlan rplan = choose_rows(c.T, c.H, c.R, 0, sms);
     const frn::StreamPlan splan = choose_stream(c.T, c.H, c.R + (c.residual ? 1 : 0), c.quant, sms);
     frn::Params p = make_params(norm, rplan, splan, nullptr);
     cudaError_t e = cudaSuccess;
@@ -808,10 +839,10 @@ FRN_EXPORT frn_status frn_plan_launch(int64_t T, int H, int R, int quant, int ha
         out->threads = (plan.groups * plan.consumer_warps + 1) * 32;
         out->grid = plan.grid;
     } else {
-        const frn::RowPlan plan = plan_rows(T, H, R, num_sms);
+        const frn::RowPlan plan = plan_rows(T, H, R, quant, num_sms);
         out->ctas_per_row = plan.ctas_per_row;
         out->rows_per_cta = plan.rows_per_cta;
-        out->tiles_per_warp = 1;
+        out->tiles_per_warp = plan.tiles_per_warp;
         out->tiles_per_cta = plan.tiles_per_cta;
         out->threads = plan.threads;
         out->grid = plan.grid;

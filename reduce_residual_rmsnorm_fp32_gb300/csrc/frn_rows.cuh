@@ -321,6 +321,129 @@ frn_row_kernel(const __grid_constant__ Params p) {
     }
 }
 
+// Rows of 33..64 tiles (8192 < H <= 16384) with few partials on one CTA of up
+// to 1024 threads: warp w takes tiles w and w + nwarps, so that the row's sum
+// of squares never leaves the CTA (no cluster exchange, no cluster to
+// schedule) while a whole row's loads are in flight on one SM.  Same per-vector
+// arithmetic, tile sums and tree as frn_row_kernel, so the same bits.
+template <int RMAX, int MODE>
+__global__ void __launch_bounds__(1024, 1) frn_row2_kernel(const __grid_constant__ Params p) {
+    __shared__ float tile_sum[kMaxTiles];
+    __shared__ float rstd_sh;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nwarps = static_cast<int>(blockDim.x >> 5);
+    const long long row = blockIdx.x;
+    int tile[2], j[2];
+    bool valid[2];
+    long long off[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        tile[t] = warp + t * nwarps;
+        j[t] = tile[t] * kTileVecs + lane;
+        valid[t] = tile[t] < p.ntiles && j[t] < p.nvec;
+        off[t] = row * static_cast<long long>(p.nvec) + j[t];
+    }
+
+    // decode-sized grids: this warp's tiles into L2 before the dependency wait
+    if (p.prefetch_l2) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            if (tile[t] < p.ntiles) prefetch_tile_span(p, row, tile[t], lane, true);
+    }
+    // many rows: the first wave's own row, and the row a fixed distance ahead
+    if (p.prefetch_ahead > 0 && warp == 0) {
+        if (row < p.prefetch_own_below) prefetch_cta_span(p, row, 1, 0, lane, true);
+        const long long ahead = row + p.prefetch_ahead;
+        if (ahead < p.T) prefetch_cta_span(p, ahead, 1, 0, lane);
+    }
+
+    grid_dependency_wait();
+
+    // every load of both tiles in flight before the first add
+    uint4 raw[2][RMAX], res[2], g[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) raw[t][r] = ld_stream(p.partials[r] + off[t], valid[t] && r < p.R);
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        res[t] = ld_coherent(p.residual + off[t], valid[t] && p.residual != nullptr);
+        g[t] = ld_keep(p.gamma + j[t], valid[t]);
+    }
+    launch_dependents();
+
+    // fp32 sum in rank order, residual last, one RNE to bf16; residual_out and
+    // the tile sums right away
+    uint4 ro[2];
+    float amax_xg[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        float acc[8];
+        unpack8(raw[t][0], acc);
+#pragma unroll
+        for (int r = 1; r < RMAX; ++r)
+            if (r < p.R) add8(acc, raw[t][r]);
+        add8(acc, res[t]);
+        ro[t] = pack8(acc);
+        const float s = tile_sumsq(ro[t]);
+        if (lane == 0 && tile[t] < p.ntiles) tile_sum[tile[t]] = s;
+        if (valid[t] && p.residual_out != nullptr) p.residual_out[off[t]] = ro[t];
+        if constexpr (mode_fp8(MODE)) {
+            float xg[8];
+            xgamma8(ro[t], g[t], xg);
+            amax_xg[t] = xgamma_group_absmax<16>(xg);
+        }
+    }
+    __syncthreads();
+    // lane k holds tile slots k and k + 32 (zeros past the row's tiles)
+    if (p.rstd_one_warp) {
+        if (warp == 0) {
+            const float lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
+            const float hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
+            const float r0 = row_rstd(lo, hi, p.H, p.eps);
+            if (lane == 0) rstd_sh = r0;
+        }
+        __syncthreads();
+    }
+    float rstd;
+    if (p.rstd_one_warp) {
+        rstd = rstd_sh;
+    } else {
+        const float lo = lane < p.ntiles ? tile_sum[lane] : 0.0f;
+        const float hi = lane + 32 < p.ntiles ? tile_sum[lane + 32] : 0.0f;
+        rstd = row_rstd(lo, hi, p.H, p.eps);
+    }
+
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        float xg[8];
+        xgamma8(ro[t], g[t], xg);
+        const uint4 yb = y_from_xgamma(xg, rstd);
+        if constexpr (mode_writes_y(MODE)) {
+            if (valid[t]) p.y[off[t]] = yb;
+        }
+        if constexpr (mode_fp8(MODE)) {
+            uint2 qq;
+            float sc;
+            quant8_amax(yb, y_absmax_from_xgamma(amax_xg[t], rstd), qq, sc);
+            if (valid[t]) {
+                p.q[off[t]] = qq;
+                if ((lane & 15) == 0) p.scales[row * (p.H / kGroup) + (j[t] >> 4)] = sc;
+            }
+        }
+        if constexpr (mode_mx(MODE)) {
+            uint32_t packed, code;
+            mxfp4_8(yb, packed, code);
+            if (valid[t]) {
+                p.q4[off[t]] = packed;
+                if ((lane & 3) == 0) p.mx_scales[row * (p.H / 32) + (j[t] >> 2)] = static_cast<uint8_t>(code);
+            }
+        }
+    }
+}
+
 struct RowPlan {
     int ctas_per_row;
     int tiles_per_cta;
@@ -328,6 +451,7 @@ struct RowPlan {
     int threads;
     long long grid;
     int staged;         // single-CTA rows with R > 8: staged partial loads (STAGED)
+    int tiles_per_warp; // 2: a row of 33..64 tiles on one CTA (frn_row2_kernel), else 1
 };
 
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads, bool STAGED = false>
@@ -371,9 +495,30 @@ cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t st
     return cudaLaunchKernelEx(&cfg, frn_row_kernel<RMAX, MODE, CLUSTER, MAXT, STAGED>, p);
 }
 
+template <int RMAX, int MODE>
+cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, frn_row2_kernel<RMAX, MODE>, p);
+}
+
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
+    // two tiles a warp: one CTA per row of 33..64 tiles, R <= 2 (the host
+    // plans nothing else)
+    if (plan.tiles_per_warp == 2) {
+        if (p.R <= 1) return launch_row2<1, MODE>(p, plan, stream, pdl);
+        return launch_row2<2, MODE>(p, plan, stream, pdl);
+    }
     // staged loads: one CTA of at most kMaxThreads per row, R > 8 (the host
     // plans nothing else)
     if (plan.staged) return launch_row_one<16, MODE, false, kMaxThreads, true>(p, plan, stream, pdl);

@@ -198,14 +198,16 @@ def test_many_row_launches_are_bit_identical(R):
     (2, 5000, 256, True),     # packed short rows, eight to a CTA
     (2, 700, 7168, False),    # no residual: R loads a row
     (8, 1171, 7168, False),
+    (8, 400, 16384, True),    # cluster rows, R > 2, from two waves on (FP8 output)
+    (4, 330, 12288, True),
 ])
 def test_prefetch_ahead_paths(R, T, H, with_residual):
     """Grids of more than one wave, where each CTA prefetches the rows a fixed
     distance ahead and the first wave its own rows before the dependency wait:
     every row against the oracle, and the same bits with every prefetch off."""
     inp = syn.make_inputs(R, T, H, seed=90 + R + T + H, partial_std=0.5, with_residual=with_residual)
-    assert frn.query_launch(T, H, R, 0, with_residual)[0] == frn.KERNEL_ROWS
     quant = H % 128 == 0 and with_residual
+    assert frn.query_launch(T, H, R, 1 if quant else 0, with_residual)[0] == frn.KERNEL_ROWS
     if quant:
         check_quant(inp, f"ahead R={R} T={T} H={H}")
     else:
@@ -219,6 +221,59 @@ def test_prefetch_ahead_paths(R, T, H, with_residual):
         frn.set_l2_prefetch(0)
     for a, b in zip(base, off):
         assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+
+
+@pytest.mark.parametrize("R,T,H,with_residual", [
+    (2, 400, 16384, True), (1, 320, 8200, True), (2, 333, 12288, True), (2, 310, 10000, True),
+    (1, 500, 16384, False), (2, 304, 8448, True),
+])
+def test_two_tiles_per_warp(R, T, H, with_residual):
+    """Rows of 33..64 tiles with R <= 2 at many rows take one CTA per row, two
+    tiles a warp: every row against the oracle, and the bits of the cluster
+    and stream kernels (and of a forced launch at decode size, prefetch on)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    quant = H % 128 == 0 and with_residual
+    plan = frn.plan_launch(T, H, R, 1 if quant else 0, with_residual, sms)
+    assert plan["kernel"] == frn.KERNEL_ROWS and plan["tiles_per_warp"] == 2, plan
+    inp = syn.make_inputs(R, T, H, seed=70 + R + T + H, partial_std=0.5, with_residual=with_residual)
+    if quant:
+        check_quant(inp, f"two tiles R={R} T={T} H={H}")
+    else:
+        check_norm(inp, f"two tiles R={R} T={T} H={H} res={with_residual}")
+    d = DevInputs(inp)
+
+    def outs():
+        got = list(gpu_quant(d, True)) if quant else list(gpu_norm(d))
+        if H % 32 == 0:
+            (q4, sc4), ro4 = frn.fused_reduce_rmsnorm_mxfp4(d.partials, d.residual, d.gamma, d.eps, False)
+            got += [host_bits(q4), host_bits(sc4), host_bits(ro4)]
+        return got
+    base = outs()
+    for kernel, ctas in ((frn.KERNEL_STREAM, 0), (frn.KERNEL_ROWS, 4)):
+        frn.set_kernel(kernel)
+        frn.set_ctas_per_row(ctas)
+        try:
+            other = outs()
+        finally:
+            frn.set_ctas_per_row(0)
+            frn.set_kernel(frn.KERNEL_AUTO)
+        for a, b in zip(base, other):
+            assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8)), (kernel, ctas)
+    # a decode-sized call forced onto the same shape, with the prefetch before the wait
+    few = DevInputs(syn.Inputs(inp.partials[:, :5], None if inp.residual is None else inp.residual[:5],
+                               inp.gamma, inp.eps))
+    frn.set_kernel(frn.KERNEL_ROWS)
+    frn.set_ctas_per_row(1)
+    frn.set_l2_prefetch(2)
+    try:
+        assert frn.plan_launch(5, H, R, 0, with_residual, sms)["tiles_per_warp"] == 2
+        ro5, y5 = gpu_norm(few)
+    finally:
+        frn.set_l2_prefetch(0)
+        frn.set_ctas_per_row(0)
+        frn.set_kernel(frn.KERNEL_AUTO)
+    ro_all, y_all = gpu_norm(d)
+    assert np.array_equal(ro5, ro_all[:5]) and np.array_equal(y5, y_all[:5])
 
 
 @pytest.mark.parametrize("H", [256, 512, 768, 1024])
