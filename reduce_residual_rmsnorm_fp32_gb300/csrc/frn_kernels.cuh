@@ -1,9 +1,11 @@
 // frn_kernels.cuh -- the two kernel families and the per-variant launchers.
 //
-//  * frn_rows.cuh   row kernel: one token row per thread-block cluster; all of
-//                   a thread's loads in flight at once; for decode-sized T.
+//  * frn_rows.cuh   row kernel: one token row per CTA, per thread-block
+//                   cluster, or several short rows per CTA; all of a thread's
+//                   loads in flight at once (in stages of two for R > 8); every
+//                   row that fits one CTA, at any T.
 //  * frn_stream.cuh stream kernel: persistent, TMA bulk copies into a shared-
-//                   memory ring, warp-specialised; for many rows.
+//                   memory ring, warp-specialised; for rows wider than one CTA.
 //  * frn_unfused.cuh the 3-kernel / 2-kernel comparison stages.
 // Both run the per-vector arithmetic of frn_common.cuh, so a row gives the
 // same bits whichever of them computes it.

@@ -1,5 +1,6 @@
 // frn_rows.cuh -- the row kernel: one token row per CTA or per thread-block
-// cluster, or several short rows per CTA.
+// cluster, or several short rows per CTA; and its two-tiles-a-warp variant
+// (frn_row2_kernel) for rows of 33..64 tiles on one CTA.
 //
 // The tiles of a row go to one CTA (up to 1024 threads) or are spread over C
 // CTAs of one cluster (tiles_per_cta warps each, one tile per warp): a row too

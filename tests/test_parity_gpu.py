@@ -383,6 +383,20 @@ def test_in_place_residual(T, H, kernel):
     assert_y_close(host_bits(y), ry, f"in place T={T} H={H} kernel={kernel}")
 
 
+@pytest.mark.parametrize("R,T,H", [(8, 16, 7168), (8, 5, 16384), (2, 400, 16384), (2, 320, 9000)])
+def test_in_place_residual_cluster_and_two_tile(R, T, H):
+    """residual_out == residual on the cluster shapes (which store residual_out
+    before the tile sums cross the cluster) and on the two-tile shape."""
+    inp = syn.make_inputs(R, T, H, seed=5, partial_std=0.5)
+    d = DevInputs(inp)
+    rro, ry = ref_norm(inp)
+    res = d.residual.clone()
+    y, ro = frn.fused_reduce_rmsnorm(d.partials, res, d.gamma, inp.eps, residual_out=res)
+    assert ro.data_ptr() == res.data_ptr()
+    assert_residual_exact(host_bits(res), rro, f"in place R={R} T={T} H={H}")
+    assert_y_close(host_bits(y), ry, f"in place R={R} T={T} H={H}")
+
+
 def test_separate_partial_allocations_and_repeats():
     """Partials as R separate tensors, including one pointer passed twice."""
     inp = syn.make_inputs(3, 9, 2048, seed=4)
