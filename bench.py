@@ -499,13 +499,14 @@ def measure_fusion(frn, R, T, Hh, seed, hbm, outlier=False, partial_std=0.5):
 def measure_e2e(frn, steps: int):
     """The decode step through the public API from pinned host memory.  Every
     step copies all of its inputs (the four T values' partials and residuals,
-    and gamma) host->device in one copy from one pinned buffer, and makes the
-    four fused calls with their outputs (residual_out and y) in pinned host
-    memory, so the kernels write the results straight over the host link (the
-    link carries about 200 GB/s either way, and a separate device->host copy
-    measured 9% slower per step).  Steps are pipelined the way a serving loop
-    would run them: two buffer sets, the next step's host->device copy on its
-    own stream while the current step computes."""
+    and gamma) host->device in one copy from one pinned buffer, makes the four
+    fused calls with their outputs (residual_out and y) in device memory, and
+    copies those device->host into pinned memory in one copy.  Steps are
+    pipelined the way a serving loop would run them: two buffer sets, each
+    copy direction on its own stream (its own copy engine), so that the next
+    step's inputs and the previous step's results cross the host link while
+    the current step computes.  Measured on GB300 against the kernels writing
+    their outputs straight into pinned host memory: 78.8 vs 84.5 us a step."""
     inps = [syn.config_decode(T, seed=500 + i) for i, T in enumerate(DECODE_T)]
     in_parts = []
     for inp in inps:
@@ -516,6 +517,7 @@ def measure_e2e(frn, steps: int):
     n_out = sum(2 * T * H for T in DECODE_T)
     host_out = [torch.empty((n_out,), dtype=torch.int16).pin_memory() for _ in range(2)]
     dev_in = [torch.empty_like(host_in, device="cuda") for _ in range(2)]
+    dev_out = [torch.empty((n_out,), dtype=torch.int16, device="cuda") for _ in range(2)]
 
     def views(di, do):
         out, off, ooff = [], 0, 0
@@ -530,13 +532,16 @@ def measure_e2e(frn, steps: int):
             out.append((p, r, ro, y))
         return out, di[off:off + H].view(torch.bfloat16)
 
-    vs = [views(dev_in[i], host_out[i]) for i in range(2)]
+    vs = [views(dev_in[i], dev_out[i]) for i in range(2)]
     h2d = host_in.numel() * 2
     d2h = host_out[0].numel() * 2
     compute = torch.cuda.current_stream()
     copy_in = torch.cuda.Stream()
+    copy_out = torch.cuda.Stream()
     loaded = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
 
     def load(buf, k):
         with torch.cuda.stream(copy_in):
@@ -547,16 +552,25 @@ def measure_e2e(frn, steps: int):
 
     def run(nsteps):
         copy_in.wait_stream(compute)          # nothing of this run starts before the caller's last op
+        copy_out.wait_stream(compute)
         load(0, 0)
         for k in range(nsteps):
             b = k % 2
             if k + 1 < nsteps:
                 load((k + 1) % 2, k + 1)
             compute.wait_event(loaded[b])
+            if k >= 2:
+                compute.wait_event(drained[b])    # step k-2's results have left this buffer
             calls, gamma_d = vs[b]
             for p, r, ro, y in calls:
                 frn.fused_reduce_rmsnorm(p, r, gamma_d, EPS, residual_out=ro, y=y)
             consumed[b].record(compute)
+            computed[b].record(compute)
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(computed[b])
+                host_out[b].copy_(dev_out[b], non_blocking=True)
+                drained[b].record(copy_out)
+        compute.wait_stream(copy_out)         # the timed region ends with the last results on the host
 
     run(4)
     torch.cuda.synchronize()
