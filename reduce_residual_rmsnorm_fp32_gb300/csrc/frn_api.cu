@@ -150,16 +150,18 @@ frn::RowPlan choose_rows(long long T, int H, int R, int quant, int num_sms) {
     } else {
         // One CTA per row (a wide one when the row needs more than 512
         // threads), or the smallest cluster that holds the row -- except for a
-        // few rows of more than 96 KB of loads each, which go to a cluster of
-        // up to 4 CTAs so that about 64 CTAs share the work (measured with the
-        // L2 prefetch at H = 4096..16384, R = 2..8, T = 8..128: larger
-        // clusters and more CTAs cost more in synchronisation than they gain).
+        // few rows of more than 96 KB of loads each, which go to clusters so
+        // that about 20 to 80 CTAs share the work: up to 7 CTAs at T <= 5, 4 up
+        // to T = 16, 2 up to T = 40 (measured with the L2 prefetch at
+        // H = 4096..16384, R = 2..8, T = 3..128; R = 8, H = 7168 in a chain
+        // of same-size calls, clusters of 1 / 2 / 4 / 7: T = 3 2.48 / 2.06 /
+        // 2.05 / 1.95 us, T = 5 2.50 / 2.08 / 2.08 / 1.86 us, T = 37 2.63 /
+        // 2.45 / 2.65 / 2.64 us, T = 45 2.65 / 2.71 / 2.81 / 2.86 us; larger
+        // clusters and more CTAs otherwise cost more in synchronisation than
+        // they gain).
         const long long row_bytes = 2LL * H * (R + 1);
         int want = 1;
-        if (row_bytes > 96 * 1024 && T < 64) {
-            want = static_cast<int>(64 / T);
-            if (want > 4) want = 4;
-        }
+        if (row_bytes > 96 * 1024) want = T <= 5 ? 7 : T <= 16 ? 4 : T <= 40 ? 2 : 1;
         if (want <= 1) {
             if (cmin > 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
             C = cmin;
