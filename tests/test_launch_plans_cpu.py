@@ -157,3 +157,14 @@ def test_staged_plans():
     assert frn.plan_launch(8192, 16384, 2, 3, True, 152)["kernel"] == frn.KERNEL_STREAM   # MXFP4 without y
     assert frn.plan_launch(8192, 10000, 1, 0, True, 152)["threads"] == 20 * 32    # 40 tiles, ragged
     assert frn.plan_launch(64, 16384, 2, 0, True, 152)["tiles_per_warp"] == 1     # few rows: clusters
+
+
+def test_cluster_sizes_for_heavy_rows():
+    """Rows of more than 96 KB of loads spread over clusters at small T (up to
+    7 CTAs at T <= 5, 4 up to T = 16, 2 up to T = 40), a divisor of the tile
+    count; lighter rows, and heavy rows from T = 41 on, keep one CTA a row."""
+    expect = {3: 7, 5: 7, 6: 4, 8: 4, 16: 4, 17: 2, 32: 2, 40: 2, 41: 1, 64: 1}
+    for T, C in expect.items():
+        assert frn.plan_launch(T, 7168, 8, 0, True, 152)["ctas_per_row"] == C, T
+    assert frn.plan_launch(3, 4096, 8, 0, True, 152)["ctas_per_row"] == 1      # 72 KB a row
+    assert frn.plan_launch(3, 16384, 2, 0, True, 152)["ctas_per_row"] == 4     # 7 does not divide 64 tiles
