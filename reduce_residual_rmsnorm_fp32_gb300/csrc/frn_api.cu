@@ -111,17 +111,20 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
-// Rows of 33..64 tiles (8192 < H <= 16384) with R <= 2 from two waves on: one
+// Rows of 33..64 tiles (8192 < H <= 16384) with R <= 4 from two waves on: one
 // CTA per row, two tiles a warp (frn_row2_kernel), instead of a cluster of
-// CTAs or the stream kernel -- except MXFP4 without y, where the stream
-// kernel (gamma in shared memory) stays ahead.  Measured on GB300 at R = 2,
-// T = 8192, H = 16384 (two-tile row / stream / clusters of 4, us): no quant
-// 192.7 / 201.2 / 244.4, FP8 A 182.3 / 287.1 / 269.5, FP8 B 213.3 / 280.4 /
-// 284.6, MXFP4 B 203.0 / 246.8 / 281.6, MXFP4 A 175.9 / 167.2 / 259.2; H =
-// 12288 FP8 A 152.9 / 173.9 / 200.7; R = 1, H = 16384 FP8 A 163.8 / 270.0 /
-// 256.0; R = 2, H = 16384, T = 600 FP8 A 18.4 / 29.5 / 23.1.
+// CTAs or the stream kernel -- except MXFP4 without y at R <= 2, where the
+// stream kernel (gamma in shared memory) stays ahead.  Measured on GB300
+// (two-tile row / stream / clusters of 4, us): R = 2, T = 8192, H = 16384 no
+// quant 192.7 / 201.2 / 244.4, FP8 A 182.3 / 287.1 / 269.5, FP8 B 213.3 /
+// 280.4 / 284.6, MXFP4 B 203.0 / 246.8 / 281.6, MXFP4 A 175.9 / 167.2 /
+// 259.2; R = 4, T = 4096, H = 16384 FP8 A 127.2 / 189.1 / 186.1, FP8 B
+// 149.6 / 189.4 / 201.3, MXFP4 A 122.8 / 134.9 / 180.1, MXFP4 B 143.4 /
+// 162.5 / 195.0, no quant 136.2 / 136.9 / 174.0; R = 3 FP8 A 108.7 / 167.7 /
+// 180.1; R = 4, T = 600 FP8 A 23.9 / 35.8 / 31.5.  With R <= 8 the doubled
+// loads would spill.
 bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
-    return ntiles > 2 * frn::kMaxTilesPerCta && R <= 2 && quant != 3 && T >= 2LL * num_sms;
+    return ntiles > 2 * frn::kMaxTilesPerCta && R <= 4 && !(quant == 3 && R <= 2) && T >= 2LL * num_sms;
 }
 
 frn::RowPlan two_tile_plan(long long T, int ntiles) {
@@ -139,7 +142,7 @@ frn::RowPlan choose_rows(long long T, int H, int R, int quant, int num_sms) {
     int C;
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
     if (forced == 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
-    if ((forced == 1 && ntiles > 2 * frn::kMaxTilesPerCta && R <= 2) ||
+    if ((forced == 1 && ntiles > 2 * frn::kMaxTilesPerCta && R <= 4) ||
         (forced == 0 && two_tile_rows(T, ntiles, R, quant, num_sms)))
         return two_tile_plan(T, ntiles);
     if (forced > 0) {

@@ -514,11 +514,12 @@ cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t strea
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
-    // two tiles a warp: one CTA per row of 33..64 tiles, R <= 2 (the host
-    // plans nothing else)
+    // two tiles a warp: one CTA per row of 33..64 tiles, R <= 4 (the host
+    // plans nothing else; R <= 8 would spill)
     if (plan.tiles_per_warp == 2) {
         if (p.R <= 1) return launch_row2<1, MODE>(p, plan, stream, pdl);
-        return launch_row2<2, MODE>(p, plan, stream, pdl);
+        if (p.R <= 2) return launch_row2<2, MODE>(p, plan, stream, pdl);
+        return launch_row2<4, MODE>(p, plan, stream, pdl);
     }
     // staged loads: one CTA of at most kMaxThreads per row, R > 8 (the host
     // plans nothing else)

@@ -199,7 +199,7 @@ def test_many_row_launches_are_bit_identical(R):
     (2, 700, 7168, False),    # no residual: R loads a row
     (8, 1171, 7168, False),
     (8, 400, 16384, True),    # cluster rows, R > 2, from two waves on (FP8 output)
-    (4, 330, 12288, True),
+    (4, 200, 12288, True),
 ])
 def test_prefetch_ahead_paths(R, T, H, with_residual):
     """Grids of more than one wave, where each CTA prefetches the rows a fixed
@@ -225,10 +225,11 @@ def test_prefetch_ahead_paths(R, T, H, with_residual):
 
 @pytest.mark.parametrize("R,T,H,with_residual", [
     (2, 400, 16384, True), (1, 320, 8200, True), (2, 333, 12288, True), (2, 310, 10000, True),
-    (1, 500, 16384, False), (2, 304, 8448, True),
+    (1, 500, 16384, False), (2, 304, 8448, True), (4, 330, 16384, True), (3, 400, 12288, True),
+    (4, 310, 9000, False),
 ])
 def test_two_tiles_per_warp(R, T, H, with_residual):
-    """Rows of 33..64 tiles with R <= 2 at many rows take one CTA per row, two
+    """Rows of 33..64 tiles with R <= 4 at many rows take one CTA per row, two
     tiles a warp: every row against the oracle, and the bits of the cluster
     and stream kernels (and of a forced launch at decode size, prefetch on)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
