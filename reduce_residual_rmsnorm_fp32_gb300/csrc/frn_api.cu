@@ -111,7 +111,7 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
-// Rows of 33..64 tiles (8192 < H <= 16384) with R <= 4 from two waves on: one
+// Rows of 33..64 tiles (8192 < H <= 16384) with R <= 4 from half a wave on: one
 // CTA per row, two tiles a warp (frn_row2_kernel), instead of a cluster of
 // CTAs or the stream kernel -- except MXFP4 without y at R <= 2, where the
 // stream kernel (gamma in shared memory) stays ahead.  Measured on GB300
@@ -121,10 +121,12 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // 259.2; R = 4, T = 4096, H = 16384 FP8 A 127.2 / 189.1 / 186.1, FP8 B
 // 149.6 / 189.4 / 201.3, MXFP4 A 122.8 / 134.9 / 180.1, MXFP4 B 143.4 /
 // 162.5 / 195.0, no quant 136.2 / 136.9 / 174.0; R = 3 FP8 A 108.7 / 167.7 /
-// 180.1; R = 4, T = 600 FP8 A 23.9 / 35.8 / 31.5.  With R <= 8 the doubled
-// loads would spill.
+// 180.1; R = 4, T = 600 FP8 A 23.9 / 35.8 / 31.5; R = 4, H = 16384, T = 80
+// no quant 4.7 / 6.7 / 6.3, R = 2 at T = 80 level with clusters (3.7 vs
+// 3.6-3.8), at T = 152 5.2 / 7.2 / 7.1.  With R <= 8 the doubled loads would
+// spill.
 bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
-    return ntiles > 2 * frn::kMaxTilesPerCta && R <= 4 && !(quant == 3 && R <= 2) && T >= 2LL * num_sms;
+    return ntiles > 2 * frn::kMaxTilesPerCta && R <= 4 && !(quant == 3 && R <= 2) && 2 * T >= num_sms;
 }
 
 frn::RowPlan two_tile_plan(long long T, int ntiles) {

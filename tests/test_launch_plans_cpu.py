@@ -27,7 +27,7 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
     what = (T, H, R, quant, residual, sms, pl)
     if auto and (ntiles <= 16 or (ntiles <= 32 and R <= 8)):
         assert pl["kernel"] == frn.KERNEL_ROWS, what                    # every row that fits one CTA
-    if auto and ntiles > 32 and R <= 4 and T >= 2 * sms and not (quant == 3 and R <= 2):
+    if auto and ntiles > 32 and R <= 4 and 2 * T >= sms and not (quant == 3 and R <= 2):
         assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, what
     if pl["kernel"] == frn.KERNEL_ROWS:
         C, tpc, rows, thr = pl["ctas_per_row"], pl["tiles_per_cta"], pl["rows_per_cta"], pl["threads"]
@@ -159,7 +159,8 @@ def test_staged_plans():
         assert frn.plan_launch(4096, 16384, R, quant, True, 152)["tiles_per_warp"] == 2, (R, quant)
     assert frn.plan_launch(4096, 16384, 5, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
     assert frn.plan_launch(8192, 10000, 1, 0, True, 152)["threads"] == 20 * 32    # 40 tiles, ragged
-    assert frn.plan_launch(64, 16384, 2, 0, True, 152)["tiles_per_warp"] == 1     # few rows: clusters
+    assert frn.plan_launch(75, 16384, 2, 0, True, 152)["tiles_per_warp"] == 1     # few rows: clusters
+    assert frn.plan_launch(76, 16384, 4, 1, True, 152)["tiles_per_warp"] == 2
 
 
 def test_cluster_sizes_for_heavy_rows():

@@ -199,7 +199,7 @@ def test_many_row_launches_are_bit_identical(R):
     (2, 700, 7168, False),    # no residual: R loads a row
     (8, 1171, 7168, False),
     (8, 400, 16384, True),    # cluster rows, R > 2, from two waves on (FP8 output)
-    (4, 200, 12288, True),
+    (6, 300, 12288, True),
 ])
 def test_prefetch_ahead_paths(R, T, H, with_residual):
     """Grids of more than one wave, where each CTA prefetches the rows a fixed
