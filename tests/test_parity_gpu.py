@@ -482,11 +482,12 @@ def test_staged_loads(R, T, H):
                 assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
 
-@pytest.mark.parametrize("R,T,H", [(2, 300, 16384), (8, 200, 12288), (1, 170, 8320)])
+@pytest.mark.parametrize("R,T,H", [(2, 60, 16384), (8, 200, 12288), (1, 70, 8320), (6, 400, 16384)])
 def test_wide_fp8_rows_on_clusters(R, T, H):
-    """FP8 output on rows wider than 8192: the planner takes the row kernel's
-    clusters (with R <= 2 and the one-wave-ahead prefetch); every row against
-    the oracle, and the same bits as the stream kernel."""
+    """FP8 output on rows wider than 8192 with R > 4, or R <= 4 below half a
+    wave: the planner takes the row kernel's clusters (with the prefetch ahead
+    from two waves on); every row against the oracle, and the same bits as the
+    stream kernel."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = frn.plan_launch(T, H, R, 1, True, sms)
     assert plan["kernel"] == frn.KERNEL_ROWS and plan["ctas_per_row"] > 1, plan
