@@ -1,10 +1,10 @@
 """MXFP4 output variant (OCP MX: 32-element blocks, E8M0 scale, E2M1 elements)
 against the oracle, under both kernels and both output variants.
 
-Matching rule: residual_out bit-exact, y within one bf16 ulp; in every block
-whose y equals the oracle's bit for bit, the E8M0 code and all E2M1 codes are
-equal; elsewhere (a 1-ulp y flip) E2M1 codes differ by at most one step, on at
-most 0.1% of all elements."""
+Matching rule: residual_out bit-exact, y within one bf16 ulp (off by one on
+at most 0.1% of elements); every block's E8M0 code and E2M1 codes equal the
+oracle's OCP MX quantisation of the library's own y, and the oracle's own codes
+wherever the block's y equals the oracle's."""
 import os
 
 import numpy as np
@@ -34,7 +34,7 @@ def check_mx(inp, what):
                                                            threads=THREADS)
     assert_residual_exact(ro, rro, what)
     assert_y_close(yb, ry, what)
-    assert_mx_close(None, host_bits(qa), host_bits(sa), ry, rq, rs, what + " (A)")
+    assert_mx_close(host_bits(y), host_bits(qa), host_bits(sa), ry, rq, rs, what + " (A)")
     return assert_mx_close(yb, q, s, ry, rq, rs, what + " (B)")
 
 
