@@ -5,6 +5,7 @@ matching rules:
 * residual_out: bit-exact (same fixed-order fp32 sum, one RNE);
 * y: within 1 bf16 ulp (|difference of ordered bit patterns| <= 1);
 * fp8 codes: equal, except at most 1 e4m3 ulp on at most 0.1% of elements;
+  and, given the library's y, exactly the oracle's quantisation of that y;
 * scales: within 1e-6 relative of the oracle wherever the group's absmax y
   element has the same bits on both sides, and for every group within 1e-6 of
   absmax(y_gpu) / 448 (the GPU's own y) -- a 1-ulp flip of the absmax y
@@ -89,6 +90,13 @@ def assert_y_close(y_gpu, y_ref, what="") -> int:
 def assert_quant_close(y_gpu, q_gpu, s_gpu, y_ref, q_ref, s_ref, what="", group=128) -> dict:
     T, H = q_ref.shape
     ng = H // group
+    if y_gpu is not None:
+        # the same decision in the same precision: the library's codes and
+        # scales are the oracle's quantisation of the library's own y
+        import oracle
+        q_y, s_y = oracle.Oracle().quant_per_group(y_gpu, group)
+        assert np.array_equal(q_gpu, q_y) and np.array_equal(s_gpu.view(np.uint32), s_y.view(np.uint32)), \
+            f"{what}: fp8 codes or scales are not the oracle's quantisation of the library's y"
     # codes
     dq = np.abs(ordered_e4m3(q_gpu) - ordered_e4m3(q_ref))
     assert dq.max(initial=0) <= Q_ULP_TOL, f"{what}: fp8 codes differ by {dq.max()} ulps"

@@ -57,6 +57,7 @@ def test_random_plan_against_oracle(case):
         roB, yB, qB, sB = gpu_quant(d, emit_bf16=True)
         assert np.array_equal(roA, ro) and np.array_equal(roB, ro) and np.array_equal(yB, y), what
         assert_quant_close(None, qA, sA, rq_y, rq, rs, what + " FP8 A")
+        assert_quant_close(y, qA, sA, rq_y, rq, rs, what + " FP8 A, the library's y")
         assert_quant_close(yB, qB, sB, rq_y, rq, rs, what + " FP8 B")
     if H % 32 == 0:
         _, mx_y, mq, ms = orc.reduce_rmsnorm_mxfp4(inp.partials, inp.residual, inp.gamma, inp.eps, threads=THREADS)
