@@ -123,10 +123,15 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // 162.5 / 195.0, no quant 136.2 / 136.9 / 174.0; R = 3 FP8 A 108.7 / 167.7 /
 // 180.1; R = 4, T = 600 FP8 A 23.9 / 35.8 / 31.5; R = 4, H = 16384, T = 80
 // no quant 4.7 / 6.7 / 6.3, R = 2 at T = 80 level with clusters (3.7 vs
-// 3.6-3.8), at T = 152 5.2 / 7.2 / 7.1.  With R <= 8 the doubled loads would
-// spill.
+// 3.6-3.8), at T = 152 5.2 / 7.2 / 7.1.  With R = 5..8 (partials loaded in
+// two stages) only for an FP8 output: R = 8, T = 2048, H = 16384 FP8 A 114.9
+// vs 125.2 us on clusters, FP8 B 121.7 vs 140.9 us, R = 6 FP8 A 94.2 vs
+// 112.3 us; without quant and with MXFP4 the stream kernel stays level or
+// ahead (R = 8 no quant 112.9 vs 113.8 us, MXFP4 A 111.2 vs 108.2 us).
 bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
-    return ntiles > 2 * frn::kMaxTilesPerCta && R <= 4 && !(quant == 3 && R <= 2) && 2 * T >= num_sms;
+    const bool fp8 = quant == 1 || quant == 2;
+    return ntiles > 2 * frn::kMaxTilesPerCta && (R <= 4 || (R <= 8 && fp8)) && !(quant == 3 && R <= 2) &&
+           2 * T >= num_sms;
 }
 
 frn::RowPlan two_tile_plan(long long T, int ntiles) {
@@ -144,7 +149,7 @@ frn::RowPlan choose_rows(long long T, int H, int R, int quant, int num_sms) {
     int C;
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
     if (forced == 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
-    if ((forced == 1 && ntiles > 2 * frn::kMaxTilesPerCta && R <= 4) ||
+    if ((forced == 1 && ntiles > 2 * frn::kMaxTilesPerCta && R <= 8) ||
         (forced == 0 && two_tile_rows(T, ntiles, R, quant, num_sms)))
         return two_tile_plan(T, ntiles);
     if (forced > 0) {

@@ -322,11 +322,13 @@ frn_row_kernel(const __grid_constant__ Params p) {
     }
 }
 
-// Rows of 33..64 tiles (8192 < H <= 16384) with few partials on one CTA of up
-// to 1024 threads: warp w takes tiles w and w + nwarps, so that the row's sum
-// of squares never leaves the CTA (no cluster exchange, no cluster to
-// schedule) while a whole row's loads are in flight on one SM.  Same per-vector
-// arithmetic, tile sums and tree as frn_row_kernel, so the same bits.
+// Rows of 33..64 tiles (8192 < H <= 16384) with up to 8 partials on one CTA
+// of up to 1024 threads: warp w takes tiles w and w + nwarps, so that the
+// row's sum of squares never leaves the CTA (no cluster exchange, no cluster
+// to schedule) while a whole row's loads are in flight on one SM (with R > 4,
+// in two stages of four partials, so that they fit 64 registers).  Same
+// per-vector arithmetic, tile sums and tree as frn_row_kernel, so the same
+// bits.
 template <int RMAX, int MODE>
 __global__ void __launch_bounds__(1024, 1) frn_row2_kernel(const __grid_constant__ Params p) {
     __shared__ float tile_sum[kMaxTiles];
@@ -361,33 +363,73 @@ __global__ void __launch_bounds__(1024, 1) frn_row2_kernel(const __grid_constant
 
     grid_dependency_wait();
 
-    // every load of both tiles in flight before the first add
-    uint4 raw[2][RMAX], res[2], g[2];
+    uint4 res[2], g[2];
+    float accs[2][8];
+    if constexpr (RMAX == 8) {
+        // two stages of four partials a tile (32 registers of loads in flight)
+        {
+            uint4 a[2][4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
+            for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int r = 0; r < RMAX; ++r) raw[t][r] = ld_stream(p.partials[r] + off[t], valid[t] && r < p.R);
+                for (int r = 0; r < 4; ++r) a[t][r] = ld_stream(p.partials[r] + off[t], valid[t] && r < p.R);
+            launch_dependents();
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                unpack8(a[t][0], accs[t]);
+#pragma unroll
+                for (int r = 1; r < 4; ++r)
+                    if (r < p.R) add8(accs[t], a[t][r]);
+            }
+        }
+        {
+            uint4 b[2][4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) b[t][r] = ld_stream(p.partials[4 + r] + off[t], valid[t] && 4 + r < p.R);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) res[t] = ld_coherent(p.residual + off[t], valid[t] && p.residual != nullptr);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (4 + r < p.R) add8(accs[t], b[t][r]);
+                add8(accs[t], res[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) g[t] = ld_keep(p.gamma + j[t], valid[t]);
+    } else {
+        // every load of both tiles in flight before the first add
+        uint4 raw[2][RMAX];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+            for (int r = 0; r < RMAX; ++r) raw[t][r] = ld_stream(p.partials[r] + off[t], valid[t] && r < p.R);
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            res[t] = ld_coherent(p.residual + off[t], valid[t] && p.residual != nullptr);
+            g[t] = ld_keep(p.gamma + j[t], valid[t]);
+        }
+        launch_dependents();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            unpack8(raw[t][0], accs[t]);
+#pragma unroll
+            for (int r = 1; r < RMAX; ++r)
+                if (r < p.R) add8(accs[t], raw[t][r]);
+            add8(accs[t], res[t]);
+        }
     }
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        res[t] = ld_coherent(p.residual + off[t], valid[t] && p.residual != nullptr);
-        g[t] = ld_keep(p.gamma + j[t], valid[t]);
-    }
-    launch_dependents();
 
-    // fp32 sum in rank order, residual last, one RNE to bf16; residual_out and
-    // the tile sums right away
+    // one RNE to bf16; residual_out and the tile sums right away
     uint4 ro[2];
     float amax_xg[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        float acc[8];
-        unpack8(raw[t][0], acc);
-#pragma unroll
-        for (int r = 1; r < RMAX; ++r)
-            if (r < p.R) add8(acc, raw[t][r]);
-        add8(acc, res[t]);
-        ro[t] = pack8(acc);
+        ro[t] = pack8(accs[t]);
         const float s = tile_sumsq(ro[t]);
         if (lane == 0 && tile[t] < p.ntiles) tile_sum[tile[t]] = s;
         if (valid[t] && p.residual_out != nullptr) p.residual_out[off[t]] = ro[t];
@@ -514,12 +556,13 @@ cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t strea
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
-    // two tiles a warp: one CTA per row of 33..64 tiles, R <= 4 (the host
-    // plans nothing else; R <= 8 would spill)
+    // two tiles a warp: one CTA per row of 33..64 tiles, R <= 8 (the host
+    // plans nothing else; R > 4 loads its partials in two stages)
     if (plan.tiles_per_warp == 2) {
         if (p.R <= 1) return launch_row2<1, MODE>(p, plan, stream, pdl);
         if (p.R <= 2) return launch_row2<2, MODE>(p, plan, stream, pdl);
-        return launch_row2<4, MODE>(p, plan, stream, pdl);
+        if (p.R <= 4) return launch_row2<4, MODE>(p, plan, stream, pdl);
+        return launch_row2<8, MODE>(p, plan, stream, pdl);
     }
     // staged loads: one CTA of at most kMaxThreads per row, R > 8 (the host
     // plans nothing else)

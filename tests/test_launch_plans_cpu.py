@@ -27,14 +27,15 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
     what = (T, H, R, quant, residual, sms, pl)
     if auto and (ntiles <= 16 or (ntiles <= 32 and R <= 8)):
         assert pl["kernel"] == frn.KERNEL_ROWS, what                    # every row that fits one CTA
-    if auto and ntiles > 32 and R <= 4 and 2 * T >= sms and not (quant == 3 and R <= 2):
+    if auto and ntiles > 32 and (R <= 4 or (R <= 8 and quant in (1, 2))) and 2 * T >= sms and \
+            not (quant == 3 and R <= 2):
         assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, what
     if pl["kernel"] == frn.KERNEL_ROWS:
         C, tpc, rows, thr = pl["ctas_per_row"], pl["tiles_per_cta"], pl["rows_per_cta"], pl["threads"]
         assert 1 <= C <= 16 and tpc >= 1 and rows >= 1, what
         assert C * tpc >= ntiles and (C - 1) * tpc < ntiles, what          # every tile, no empty CTA
         if pl["tiles_per_warp"] == 2:                                      # two tiles a warp, one CTA a row
-            assert C == 1 and rows == 1 and R <= 4 and 32 < tpc <= 64, what
+            assert C == 1 and rows == 1 and (R <= 4 or (R <= 8 and quant in (1, 2))) and 32 < tpc <= 64, what
             assert thr == -(-tpc // 2) * 32 and not pl["staged"], what
         else:
             assert pl["tiles_per_warp"] == 1 and thr == rows * tpc * 32 and thr <= 1024, what
@@ -158,6 +159,9 @@ def test_staged_plans():
     for R, quant in ((3, 0), (4, 1), (4, 3), (4, 4)):
         assert frn.plan_launch(4096, 16384, R, quant, True, 152)["tiles_per_warp"] == 2, (R, quant)
     assert frn.plan_launch(4096, 16384, 5, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
+    for R in (5, 8):   # R = 5..8 in two stages, with an FP8 output only
+        assert frn.plan_launch(2048, 16384, R, 2, True, 152)["tiles_per_warp"] == 2
+        assert frn.plan_launch(2048, 16384, R, 4, True, 152)["kernel"] == frn.KERNEL_STREAM
     assert frn.plan_launch(8192, 10000, 1, 0, True, 152)["threads"] == 20 * 32    # 40 tiles, ragged
     assert frn.plan_launch(75, 16384, 2, 0, True, 152)["tiles_per_warp"] == 1     # few rows: clusters
     assert frn.plan_launch(76, 16384, 4, 1, True, 152)["tiles_per_warp"] == 2

@@ -198,8 +198,8 @@ def test_many_row_launches_are_bit_identical(R):
     (2, 5000, 256, True),     # packed short rows, eight to a CTA
     (2, 700, 7168, False),    # no residual: R loads a row
     (8, 1171, 7168, False),
-    (8, 400, 16384, True),    # cluster rows, R > 2, from two waves on (FP8 output)
-    (6, 300, 12288, True),
+    (12, 400, 16384, True),   # cluster rows, R > 8, from two waves on (FP8 output)
+    (8, 400, 16384, True),    # two tiles a warp, partials in two stages (FP8 output)
 ])
 def test_prefetch_ahead_paths(R, T, H, with_residual):
     """Grids of more than one wave, where each CTA prefetches the rows a fixed
@@ -226,7 +226,7 @@ def test_prefetch_ahead_paths(R, T, H, with_residual):
 @pytest.mark.parametrize("R,T,H,with_residual", [
     (2, 400, 16384, True), (1, 320, 8200, True), (2, 333, 12288, True), (2, 310, 10000, True),
     (1, 500, 16384, False), (2, 304, 8448, True), (4, 330, 16384, True), (3, 400, 12288, True),
-    (4, 310, 9000, False),
+    (4, 310, 9000, False), (8, 330, 16384, True), (6, 300, 12288, True), (5, 200, 8448, True),
 ])
 def test_two_tiles_per_warp(R, T, H, with_residual):
     """Rows of 33..64 tiles with R <= 4 at many rows take one CTA per row, two
@@ -482,12 +482,12 @@ def test_staged_loads(R, T, H):
                 assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
 
-@pytest.mark.parametrize("R,T,H", [(2, 60, 16384), (8, 200, 12288), (1, 70, 8320), (6, 400, 16384)])
+@pytest.mark.parametrize("R,T,H", [(2, 60, 16384), (8, 60, 12288), (1, 70, 8320), (12, 400, 16384)])
 def test_wide_fp8_rows_on_clusters(R, T, H):
-    """FP8 output on rows wider than 8192 with R > 4, or R <= 4 below half a
-    wave: the planner takes the row kernel's clusters (with the prefetch ahead
-    from two waves on); every row against the oracle, and the same bits as the
-    stream kernel."""
+    """FP8 output on rows wider than 8192 below half a wave, or with R > 8: the
+    planner takes the row kernel's clusters (with the prefetch ahead from two
+    waves on); every row against the oracle, and the same bits as the stream
+    kernel."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = frn.plan_launch(T, H, R, 1, True, sms)
     assert plan["kernel"] == frn.KERNEL_ROWS and plan["ctas_per_row"] > 1, plan
