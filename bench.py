@@ -710,6 +710,7 @@ PROFILE_CASES = {
     "stream_R8_T1024_H16384": (8, 1024, 16384, "norm", False, 0.5),
     "R2_T2048_H16384_quant_a": (2, 2048, 16384, "quant_a", True, 1.0),
     "R4_T2048_H16384_quant_b": (4, 2048, 16384, "quant_b", False, 0.5),
+    "R8_T1024_H16384_quant_a": (8, 1024, 16384, "quant_a", False, 0.5),
     "sweep64M": (8, syn.sweep_tokens(64 << 20), H, "norm", False, 0.5),
     "sweep16M": (8, syn.sweep_tokens(16 << 20), H, "norm", False, 0.5),
     "sweep8M": (8, syn.sweep_tokens(8 << 20), H, "norm", False, 0.5),
