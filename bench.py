@@ -718,6 +718,7 @@ PROFILE_CASES = {
     "prefill_quant_b": (2, 8192, H, "quant_b", True, 1.0),
     "quant_R4_T32": (4, 32, 4096, "quant_b", False, 0.5),
     "prefill_mx_a": (2, 8192, H, "mx_a", True, 1.0),
+    "R4_T1171_H7168_quant_a": (4, 1171, H, "quant_a", False, 0.5),
 }
 
 

@@ -128,10 +128,28 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // vs 125.2 us on clusters, FP8 B 121.7 vs 140.9 us, R = 6 FP8 A 94.2 vs
 // 112.3 us; without quant and with MXFP4 the stream kernel stays level or
 // ahead (R = 8 no quant 112.9 vs 113.8 us, MXFP4 A 111.2 vs 108.2 us).
+//
+// Rows of 26..32 tiles (6144 < H <= 8192) with R = 3 or 4 beyond one row per
+// SM: the wide CTA (832..1024 threads at 40 registers) leaves room for one
+// row an SM, two-tile CTAs of half as many threads for two, so twice the
+// loads are in flight.  Measured on GB300 (two-tile / wide, us): H = 7168,
+// R = 4, T = 160 4.02 / 4.78, T = 304 6.01 / 6.90, FP8 A 6.13 / 7.16, T = 1171
+// 19.95 / 20.74, FP8 A 20.12 / 22.38, MXFP4 B 21.16 / 22.84, T = 4096 62.3 /
+// 63.5, FP8 B 68.7 / 72.8, MXFP4 A 56.2 / 65.6; R = 3, T = 304 5.18 / 6.32,
+// T = 1171 FP8 A 17.5 / 20.0; H = 8192, R = 4, T = 304 6.71 / 7.29, T = 1171
+// FP8 A 22.0 / 24.6 (no quant at T = 4096 72.0 / 70.4, the one loss).  At
+// H <= 6144 two wide CTAs fit an SM and it gains nothing (H = 6144, R = 4,
+// T = 1171 17.65 / 17.32); within one row per SM the wide CTA's extra warps
+// win (H = 7168, R = 4, T = 64 2.44 / 2.35, T = 147 3.56 / 3.47).  With R = 2
+// only FP8 A at 16 rows an SM and more (T = 8192, H = 7168 79.9 / 81.3; no
+// quant, FP8 B and MXFP4 level; T = 586 8.63 / 8.50).
 bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
     const bool fp8 = quant == 1 || quant == 2;
-    return ntiles > 2 * frn::kMaxTilesPerCta && (R <= 4 || (R <= 8 && fp8)) && !(quant == 3 && R <= 2) &&
-           2 * T >= num_sms;
+    if (ntiles > 2 * frn::kMaxTilesPerCta)
+        return (R <= 4 || (R <= 8 && fp8)) && !(quant == 3 && R <= 2) && 2 * T >= num_sms;
+    if (ntiles >= 26)
+        return ((R == 3 || R == 4) && T > num_sms) || (R == 2 && quant == 1 && T >= 16LL * num_sms);
+    return false;
 }
 
 frn::RowPlan two_tile_plan(long long T, int ntiles) {
@@ -474,7 +492,11 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // CTAs of a row-kernel launch resident on one SM: by threads (2048), CTAs
 // (32) and the registers the kernel's launch bound holds (row_min_blocks).
 long long row_ctas_per_sm(const frn::RowPlan& plan, int R) {
-    if (plan.tiles_per_warp == 2) return 1;   // frn_row2_kernel: launch bound (1024, 1), up to 1024 threads
+    if (plan.tiles_per_warp == 2) {
+        // frn_row2_kernel: launch bound (1024, 1), so up to 64 registers a thread
+        const long long by_threads = 2048 / plan.threads, by_regs = 65536 / (plan.threads * 64LL);
+        return by_threads < by_regs ? by_threads : by_regs;
+    }
     const bool cluster = plan.ctas_per_row > 1;
     const int maxt = plan.rows_per_cta > 1 ? frn::kPackedThreads : (plan.threads > frn::kMaxThreads ? 1024 : frn::kMaxThreads);
     const int rmax = R <= 1 ? 1 : R <= 2 ? 2 : R <= 4 ? 4 : R <= 8 ? 8 : 16;
@@ -505,11 +527,12 @@ long long ahead_rows(long long wave_rows, int rows_per_cta, int H, int nloads) {
 
 bool prefetch_pays(const frn::RowPlan& plan, long long T, int H, int R, int sms) {
     if (plan.grid * plan.threads > 2048LL * sms || plan.rows_per_cta > 1) return false;
-    // Wide rows: only when the registers hold the whole grid at once too (one
-    // or two rows an SM); beyond, the prefetch ahead takes over (R = 8,
+    // Wide and two-tile rows: only when the registers hold the whole grid at
+    // once too (one or two rows an SM); beyond, the prefetch ahead takes over (R = 8,
     // H = 7168: T = 250 8.5 -> 8.0 us, T = 293 9.65 -> 9.1 us, T = 347
     // 12.3 -> 11.55 us).
-    if (plan.threads > frn::kMaxThreads && plan.ctas_per_row == 1 && plan.grid > row_ctas_per_sm(plan, R) * sms)
+    if ((plan.threads > frn::kMaxThreads || plan.tiles_per_warp == 2) && plan.ctas_per_row == 1 &&
+        plan.grid > row_ctas_per_sm(plan, R) * sms)
         return false;
     const long long row_bytes = 2LL * H * (R + 1);
     if (plan.ctas_per_row == 1) return row_bytes >= 32 * 1024;
@@ -535,7 +558,7 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // T = 8192, H = 7168, R = 2; +2% at T = 32, where it is left off).
     p.rstd_one_warp = kind == kRows && rplan.grid * rplan.threads > 2048LL * sms;
     // More rows than one wave holds, with R <= 2 (few loads in flight per SM)
-    // or for wide rows: each CTA prefetches its span of the rows a fixed
+    // or for wide and two-tile rows: each CTA prefetches its span of the rows a fixed
     // distance ahead (ahead_rows), one bulk request per input, and the first
     // wave's CTAs their own span before the dependency wait.  Measured on
     // GB300 at R = 2, H = 7168: +6% at T = 8192 without quant, +4..5% at
@@ -549,7 +572,8 @@ frn_status launch_fused(const Call& c, int quant, int sms, frn_stream_t stream) 
     // overlaps the previous kernel's tail: R = 8, T = 1171 31.7 -> 30.5 us,
     // T = 2341 58.4 -> 57.2 us.
     const long long wave_rows = row_ctas_per_sm(rplan, c.R) * sms * rplan.rows_per_cta / rplan.ctas_per_row;
-    const bool wide = rplan.threads > frn::kMaxThreads && rplan.ctas_per_row == 1 && !rplan.staged;
+    const bool wide = (rplan.threads > frn::kMaxThreads || rplan.tiles_per_warp == 2) && rplan.ctas_per_row == 1 &&
+                      !rplan.staged;
     const bool cluster_waves = rplan.ctas_per_row > 1 && c.T >= 2 * wave_rows;
     if (kind == kRows && pf != 1 && (c.R <= 2 || wide || cluster_waves)) {
         if (wave_rows > 0 && c.T > wave_rows) {

@@ -3,9 +3,12 @@
 //  * frn_rows.cuh   row kernel: one token row per CTA, per thread-block
 //                   cluster, or several short rows per CTA; all of a thread's
 //                   loads in flight at once (in stages of two for R > 8); every
-//                   row that fits one CTA, at any T.
+//                   row that fits one CTA, at any T.  Its two-tiles-a-warp
+//                   variant holds a row of 26..64 tiles on one CTA at many
+//                   rows (R <= 4, or up to 8 with an FP8 output).
 //  * frn_stream.cuh stream kernel: persistent, TMA bulk copies into a shared-
-//                   memory ring, warp-specialised; for rows wider than one CTA.
+//                   memory ring, warp-specialised; for the other rows wider
+//                   than one CTA.
 //  * frn_unfused.cuh the 3-kernel / 2-kernel comparison stages.
 // Both run the per-vector arithmetic of frn_common.cuh, so a row gives the
 // same bits whichever of them computes it.

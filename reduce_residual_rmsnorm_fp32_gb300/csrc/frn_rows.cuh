@@ -1,6 +1,6 @@
 // frn_rows.cuh -- the row kernel: one token row per CTA or per thread-block
 // cluster, or several short rows per CTA; and its two-tiles-a-warp variant
-// (frn_row2_kernel) for rows of 33..64 tiles on one CTA.
+// (frn_row2_kernel) for rows of 26..64 tiles on one CTA.
 //
 // The tiles of a row go to one CTA (up to 1024 threads) or are spread over C
 // CTAs of one cluster (tiles_per_cta warps each, one tile per warp): a row too
@@ -326,7 +326,9 @@ frn_row_kernel(const __grid_constant__ Params p) {
 // of up to 1024 threads: warp w takes tiles w and w + nwarps, so that the
 // row's sum of squares never leaves the CTA (no cluster exchange, no cluster
 // to schedule) while a whole row's loads are in flight on one SM (with R > 4,
-// in two stages of four partials, so that they fit 64 registers).  Same
+// in two stages of four partials, so that they fit 64 registers).  Rows of
+// 26..32 tiles take it too with R = 2..4 at many rows: at up to 512 threads
+// two rows fit an SM, where the one-tile-a-warp CTA leaves room for one.  Same
 // per-vector arithmetic, tile sums and tree as frn_row_kernel, so the same
 // bits.
 template <int RMAX, int MODE>
@@ -494,7 +496,7 @@ struct RowPlan {
     int threads;
     long long grid;
     int staged;         // single-CTA rows with R > 8: staged partial loads (STAGED)
-    int tiles_per_warp; // 2: a row of 33..64 tiles on one CTA (frn_row2_kernel), else 1
+    int tiles_per_warp; // 2: a row on one CTA, two tiles a warp (frn_row2_kernel), else 1
 };
 
 template <int RMAX, int MODE, bool CLUSTER, int MAXT = kMaxThreads, bool STAGED = false>
@@ -556,7 +558,7 @@ cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t strea
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
-    // two tiles a warp: one CTA per row of 33..64 tiles, R <= 8 (the host
+    // two tiles a warp: one CTA per row of 26..64 tiles, R <= 8 (the host
     // plans nothing else; R > 4 loads its partials in two stages)
     if (plan.tiles_per_warp == 2) {
         if (p.R <= 1) return launch_row2<1, MODE>(p, plan, stream, pdl);

@@ -30,12 +30,16 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
     if auto and ntiles > 32 and (R <= 4 or (R <= 8 and quant in (1, 2))) and 2 * T >= sms and \
             not (quant == 3 and R <= 2):
         assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, what
+    if auto and 17 <= ntiles <= 32 and R <= 8:                          # rows a wide CTA could hold
+        two = ntiles >= 26 and ((R in (3, 4) and T > sms) or (R == 2 and quant == 1 and T >= 16 * sms))
+        assert pl["tiles_per_warp"] == (2 if two else 1), what
     if pl["kernel"] == frn.KERNEL_ROWS:
         C, tpc, rows, thr = pl["ctas_per_row"], pl["tiles_per_cta"], pl["rows_per_cta"], pl["threads"]
         assert 1 <= C <= 16 and tpc >= 1 and rows >= 1, what
         assert C * tpc >= ntiles and (C - 1) * tpc < ntiles, what          # every tile, no empty CTA
         if pl["tiles_per_warp"] == 2:                                      # two tiles a warp, one CTA a row
-            assert C == 1 and rows == 1 and (R <= 4 or (R <= 8 and quant in (1, 2))) and 32 < tpc <= 64, what
+            assert C == 1 and rows == 1 and (R <= 4 or (R <= 8 and quant in (1, 2))) and tpc <= 64, what
+            assert tpc > 32 or (tpc >= 26 and 2 <= R <= 4), what
             assert thr == -(-tpc // 2) * 32 and not pl["staged"], what
         else:
             assert pl["tiles_per_warp"] == 1 and thr == rows * tpc * 32 and thr <= 1024, what
@@ -138,14 +142,24 @@ def test_query_launch_checks_sizes_then_needs_a_device():
 def test_staged_plans():
     """Staged partial loads where they measured faster: R > 8 rows of up to 16
     tiles from three waves.  Wide rows (17-32 tiles, R <= 8) take the row
-    kernel with every output at every T, loading all partials at once."""
+    kernel with every output at every T, loading all partials at once: a wide
+    CTA a row, or, for 26..32 tiles with R = 3 or 4 beyond one row per SM,
+    two tiles a warp on half the threads."""
     pl = frn.plan_launch(600, 4096, 16, 0, True, 152)
     assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 1 and pl["threads"] == 512
     assert frn.plan_launch(300, 4096, 16, 0, True, 152)["staged"] == 0
     for quant in (0, 1, 2, 3, 4):
-        for R, T in ((8, 586), (8, 1000), (5, 586), (4, 1519), (8, 1063), (8, 4682), (3, 1171)):
+        for R, T in ((8, 586), (8, 1000), (5, 586), (4, 1519), (8, 1063), (8, 4682), (3, 1171), (4, 152)):
             pl = frn.plan_launch(T, 7168, R, quant, True, 152)
-            assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 0 and pl["threads"] == 896, (R, T, quant)
+            two = R <= 4 and T > 152
+            assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 0, (R, T, quant)
+            assert pl["threads"] == (448 if two else 896) and pl["tiles_per_warp"] == (2 if two else 1), (R, T, quant)
+        # R = 2: two tiles a warp only with an FP8 output without y from 16 rows an SM
+        assert frn.plan_launch(2432, 7168, 2, quant, True, 152)["tiles_per_warp"] == (2 if quant == 1 else 1)
+        assert frn.plan_launch(2431, 7168, 2, quant, True, 152)["tiles_per_warp"] == 1
+        # 25 tiles or fewer: two wide CTAs already fit an SM
+        assert frn.plan_launch(1171, 6400, 4, quant, True, 152)["tiles_per_warp"] == 1
+        assert frn.plan_launch(1171, 6656, 4, quant, True, 152)["threads"] == 13 * 32
     # rows wider than one CTA: the stream kernel from one row per SM (not with FP8)
     assert frn.plan_launch(1000, 16384, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
     assert frn.plan_launch(1000, 16384, 8, 3, True, 152)["kernel"] == frn.KERNEL_STREAM
