@@ -111,7 +111,7 @@ frn::RowPlan wide_plan(long long T, int ntiles) {
 
 bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCta && R <= 8; }
 
-// Rows of 33..64 tiles (8192 < H <= 16384) with R <= 4 from half a wave on: one
+// Rows of 33..64 tiles (8192 < H <= 16384) with R <= 8 from half a wave on: one
 // CTA per row, two tiles a warp (frn_row2_kernel), instead of a cluster of
 // CTAs or the stream kernel -- except MXFP4 without y at R <= 2, where the
 // stream kernel (gamma in shared memory) stays ahead.  Measured on GB300
@@ -124,10 +124,25 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // 180.1; R = 4, T = 600 FP8 A 23.9 / 35.8 / 31.5; R = 4, H = 16384, T = 80
 // no quant 4.7 / 6.7 / 6.3, R = 2 at T = 80 level with clusters (3.7 vs
 // 3.6-3.8), at T = 152 5.2 / 7.2 / 7.1.  With R = 5..8 (partials loaded in
-// two stages) only for an FP8 output: R = 8, T = 2048, H = 16384 FP8 A 114.9
-// vs 125.2 us on clusters, FP8 B 121.7 vs 140.9 us, R = 6 FP8 A 94.2 vs
-// 112.3 us; without quant and with MXFP4 the stream kernel stays level or
-// ahead (R = 8 no quant 112.9 vs 113.8 us, MXFP4 A 111.2 vs 108.2 us).
+// stages of four), two-tile / clusters of 4 with an FP8 output: R = 8,
+// T = 2048, H = 16384 FP8 A 109.9 / 125.2 us, FP8 B 119.6 / 140.9 us; two-tile
+// / stream otherwise: R = 8 MXFP4 A 105.5 / 108.0 us, MXFP4 B 114.3 / 118.3
+// us, no quant 110.2 / 109.8 us (T = 200 14.9 / 16.8 us, T = 800 47.6 /
+// 49.3 us), H = 12288 no quant 85.8 / 88.7 us, R = 7 no quant 100.9 / 104.8
+// us, R = 5 82.2 / 87.6 us (R = 6 no quant 94.1 / 91.1 us, the one loss).
+//
+// Rows of 17..32 tiles with R > 8, which no one-tile-a-warp CTA holds: two
+// tiles a warp in stages of four partials instead of clusters with an FP8
+// output (R = 16, T = 1379, H = 5120 FP8 A 46.7 / 49.1 us; R = 12, H = 8192,
+// T = 1092 FP8 A 45.7 / 57.6 us) and of the stream kernel otherwise up to 22
+// tiles, where a ring slot of R + 1 slices leaves the stream kernel one row
+// in flight an SM (R = 16, T = 1379, H = 5120 no quant 47.9 / 54.3 us, MXFP4
+// B 48.4 / 55.2 us; H = 5632 48.5 / 51.2 us).  Wider, the stream kernel keeps
+// more rows in flight and wins without FP8 (R = 16, H = 7168, T = 985 49.1 /
+// 45.5 us; H = 6144 48.1 / 46.3 us).  Rows of 33..64 tiles with R > 8: the
+// same with an FP8 output (R = 16, T = 431, H = 16384 FP8 A 48.1 / 55.8 us
+// on clusters of 4; R = 12, H = 12288 FP8 B 50.7 / 63.9 us), the stream
+// kernel otherwise (no quant 48.9 / 46.1 us).
 //
 // Rows of 26..32 tiles (6144 < H <= 8192) with R = 3 or 4 beyond one row per
 // SM: the wide CTA (832..1024 threads at 40 registers) leaves room for one
@@ -145,8 +160,9 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // quant, FP8 B and MXFP4 level; T = 586 8.63 / 8.50).
 bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
     const bool fp8 = quant == 1 || quant == 2;
-    if (ntiles > 2 * frn::kMaxTilesPerCta)
-        return (R <= 4 || (R <= 8 && fp8)) && !(quant == 3 && R <= 2) && 2 * T >= num_sms;
+    if (ntiles <= frn::kMaxTilesPerCta) return false;
+    if (R > 8) return (fp8 || ntiles <= 22) && 2 * T >= num_sms;
+    if (ntiles > 2 * frn::kMaxTilesPerCta) return !(quant == 3 && R <= 2) && 2 * T >= num_sms;
     if (ntiles >= 26)
         return ((R == 3 || R == 4) && T > num_sms) || (R == 2 && quant == 1 && T >= 16LL * num_sms);
     return false;
@@ -167,7 +183,7 @@ frn::RowPlan choose_rows(long long T, int H, int R, int quant, int num_sms) {
     int C;
     const int forced = g_force_ctas.load(std::memory_order_relaxed);
     if (forced == 1 && wide_possible(ntiles, R)) return wide_plan(T, ntiles);
-    if ((forced == 1 && ntiles > 2 * frn::kMaxTilesPerCta && R <= 8) ||
+    if ((forced == 1 && ntiles > 2 * frn::kMaxTilesPerCta) ||
         (forced == 0 && two_tile_rows(T, ntiles, R, quant, num_sms)))
         return two_tile_plan(T, ntiles);
     if (forced > 0) {
@@ -296,16 +312,17 @@ frn::StreamPlan choose_stream(long long T, int H, int nslices, int quant, int nu
 //    MXFP4 B 17.8 vs 18.5; T = 880 23.5 vs 25.1 us; H = 8192, T = 586
 //    19.0 vs 21.1 us; H = 5120 13.5 vs 15.6 us; R = 4, H = 8192, T = 1171
 //    23.2 vs 24.0 us; R = 3, H = 7168, T = 1171 18.8 vs 19.7 us;
-//  * a wider row: the stream kernel from one row per SM on, the row kernel's
-//    clusters with an FP8 output.
+//  * a wider row, or one with R > 8: the two-tile row kernel where
+//    two_tile_rows says so; else the stream kernel from one row per SM on,
+//    the row kernel's clusters with an FP8 output.
 int choose_kind(long long T, int H, int R, int quant, int num_sms) {
     const int forced = g_force_kernel.load(std::memory_order_relaxed);
     if (forced == kRows || forced == kStream) return forced;
     const int ntiles = ceil_div(H / frn::kVecElems, frn::kTileVecs);
     if (ntiles <= frn::kMaxTilesPerCta || wide_possible(ntiles, R)) return kRows;
     if (two_tile_rows(T, ntiles, R, quant, num_sms)) return kRows;
-    // Wider rows: the stream kernel from one row per SM on -- except with an
-    // FP8 output, where its single consumer group's quant epilogue, which
+    // The other wider rows: the stream kernel from one row per SM on -- except
+    // with an FP8 output, where its single consumer group's quant epilogue, which
     // nothing overlaps, is slower than the row kernel's clusters (R = 2,
     // T = 8192: H = 16384 FP8 A 266 vs 289 us, FP8 B 283 vs 287 us; H = 12288
     // FP8 A 203 vs 220 us; R = 8, T = 2048, H = 16384 FP8 A 136 vs 151 us;

@@ -322,13 +322,14 @@ frn_row_kernel(const __grid_constant__ Params p) {
     }
 }
 
-// Rows of 33..64 tiles (8192 < H <= 16384) with up to 8 partials on one CTA
-// of up to 1024 threads: warp w takes tiles w and w + nwarps, so that the
-// row's sum of squares never leaves the CTA (no cluster exchange, no cluster
-// to schedule) while a whole row's loads are in flight on one SM (with R > 4,
-// in two stages of four partials, so that they fit 64 registers).  Rows of
-// 26..32 tiles take it too with R = 2..4 at many rows: at up to 512 threads
-// two rows fit an SM, where the one-tile-a-warp CTA leaves room for one.  Same
+// Rows of 33..64 tiles (8192 < H <= 16384) on one CTA of up to 1024
+// threads: warp w takes tiles w and w + nwarps, so that the row's sum of
+// squares never leaves the CTA (no cluster exchange, no cluster to schedule)
+// while a whole row's loads are in flight on one SM (with R > 4, in stages of
+// four partials, so that they fit 64 registers).  Rows of 26..32 tiles take it
+// too with R = 2..4 at many rows (at up to 512 threads two rows fit an SM,
+// where the one-tile-a-warp CTA leaves room for one), and rows of 17..32 tiles
+// with R > 8, which no one-tile-a-warp CTA holds in registers.  Same
 // per-vector arithmetic, tile sums and tree as frn_row_kernel, so the same
 // bits.
 template <int RMAX, int MODE>
@@ -367,14 +368,19 @@ __global__ void __launch_bounds__(1024, 1) frn_row2_kernel(const __grid_constant
 
     uint4 res[2], g[2];
     float accs[2][8];
-    if constexpr (RMAX == 8) {
-        // two stages of four partials a tile (32 registers of loads in flight)
+    if constexpr (RMAX >= 8) {
+        // stages of four partials a tile (32 registers of loads in flight);
+        // the residual comes with the stage that holds the last partial
         {
             uint4 a[2][4];
 #pragma unroll
             for (int t = 0; t < 2; ++t)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) a[t][r] = ld_stream(p.partials[r] + off[t], valid[t] && r < p.R);
+            if (p.R <= 4) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) res[t] = ld_coherent(p.residual + off[t], valid[t] && p.residual != nullptr);
+            }
             launch_dependents();
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -384,24 +390,31 @@ __global__ void __launch_bounds__(1024, 1) frn_row2_kernel(const __grid_constant
                     if (r < p.R) add8(accs[t], a[t][r]);
             }
         }
-        {
+#pragma unroll
+        for (int s = 1; s < RMAX / 4; ++s) {
+            if (4 * s >= p.R) break;
             uint4 b[2][4];
 #pragma unroll
             for (int t = 0; t < 2; ++t)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) b[t][r] = ld_stream(p.partials[4 + r] + off[t], valid[t] && 4 + r < p.R);
+                for (int r = 0; r < 4; ++r)
+                    b[t][r] = ld_stream(p.partials[4 * s + r] + off[t], valid[t] && 4 * s + r < p.R);
+            if (4 * s + 4 >= p.R) {
 #pragma unroll
-            for (int t = 0; t < 2; ++t) res[t] = ld_coherent(p.residual + off[t], valid[t] && p.residual != nullptr);
+                for (int t = 0; t < 2; ++t) res[t] = ld_coherent(p.residual + off[t], valid[t] && p.residual != nullptr);
+            }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
-                    if (4 + r < p.R) add8(accs[t], b[t][r]);
-                add8(accs[t], res[t]);
+                    if (4 * s + r < p.R) add8(accs[t], b[t][r]);
             }
         }
 #pragma unroll
-        for (int t = 0; t < 2; ++t) g[t] = ld_keep(p.gamma + j[t], valid[t]);
+        for (int t = 0; t < 2; ++t) {
+            add8(accs[t], res[t]);
+            g[t] = ld_keep(p.gamma + j[t], valid[t]);
+        }
     } else {
         // every load of both tiles in flight before the first add
         uint4 raw[2][RMAX];
@@ -558,13 +571,14 @@ cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t strea
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
-    // two tiles a warp: one CTA per row of 26..64 tiles, R <= 8 (the host
-    // plans nothing else; R > 4 loads its partials in two stages)
+    // two tiles a warp: one CTA per row of 17..64 tiles (the host plans
+    // nothing else; R > 4 loads its partials in stages of four)
     if (plan.tiles_per_warp == 2) {
         if (p.R <= 1) return launch_row2<1, MODE>(p, plan, stream, pdl);
         if (p.R <= 2) return launch_row2<2, MODE>(p, plan, stream, pdl);
         if (p.R <= 4) return launch_row2<4, MODE>(p, plan, stream, pdl);
-        return launch_row2<8, MODE>(p, plan, stream, pdl);
+        if (p.R <= 8) return launch_row2<8, MODE>(p, plan, stream, pdl);
+        return launch_row2<16, MODE>(p, plan, stream, pdl);
     }
     // staged loads: one CTA of at most kMaxThreads per row, R > 8 (the host
     // plans nothing else)

@@ -27,9 +27,14 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
     what = (T, H, R, quant, residual, sms, pl)
     if auto and (ntiles <= 16 or (ntiles <= 32 and R <= 8)):
         assert pl["kernel"] == frn.KERNEL_ROWS, what                    # every row that fits one CTA
-    if auto and ntiles > 32 and (R <= 4 or (R <= 8 and quant in (1, 2))) and 2 * T >= sms and \
-            not (quant == 3 and R <= 2):
+    if auto and ntiles > 32 and R <= 8 and 2 * T >= sms and not (quant == 3 and R <= 2):
         assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, what
+    if auto and ntiles > 16 and R > 8:                                  # no one-tile-a-warp CTA holds the row
+        two = (quant in (1, 2) or ntiles <= 22) and 2 * T >= sms
+        if two:
+            assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, what
+        else:
+            assert pl["kernel"] == frn.KERNEL_STREAM or pl["tiles_per_warp"] == 1, what
     if auto and 17 <= ntiles <= 32 and R <= 8:                          # rows a wide CTA could hold
         two = ntiles >= 26 and ((R in (3, 4) and T > sms) or (R == 2 and quant == 1 and T >= 16 * sms))
         assert pl["tiles_per_warp"] == (2 if two else 1), what
@@ -38,16 +43,16 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
         assert 1 <= C <= 16 and tpc >= 1 and rows >= 1, what
         assert C * tpc >= ntiles and (C - 1) * tpc < ntiles, what          # every tile, no empty CTA
         if pl["tiles_per_warp"] == 2:                                      # two tiles a warp, one CTA a row
-            assert C == 1 and rows == 1 and (R <= 4 or (R <= 8 and quant in (1, 2))) and tpc <= 64, what
-            assert tpc > 32 or (tpc >= 26 and 2 <= R <= 4), what
+            assert C == 1 and rows == 1 and tpc <= 64, what
+            assert tpc > 32 or (tpc >= 26 and 2 <= R <= 4) or (tpc > 16 and R > 8), what
             assert thr == -(-tpc // 2) * 32 and not pl["staged"], what
         else:
             assert pl["tiles_per_warp"] == 1 and thr == rows * tpc * 32 and thr <= 1024, what
         assert tpc <= (64 if pl["tiles_per_warp"] == 2 else 32), what     # per-CTA tile-sum slots
         if rows > 1:                                                       # packed 256-thread variant
             assert C == 1 and tpc == ntiles and thr <= 256, what
-        if thr > 512:                                                      # wide variant: one CTA, R <= 8
-            assert C == 1 and rows == 1 and R <= 8, what
+        if thr > 512:                                                      # wide or two-tile: one CTA
+            assert C == 1 and rows == 1 and (R <= 8 or pl["tiles_per_warp"] == 2), what
         if C > 1:                                                          # cluster variant: <= 512 threads
             assert thr <= 512 and rows == 1 and C <= 8, what
         assert pl["grid"] == -(-T // rows) * C, what
@@ -160,22 +165,28 @@ def test_staged_plans():
         # 25 tiles or fewer: two wide CTAs already fit an SM
         assert frn.plan_launch(1171, 6400, 4, quant, True, 152)["tiles_per_warp"] == 1
         assert frn.plan_launch(1171, 6656, 4, quant, True, 152)["threads"] == 13 * 32
-    # rows wider than one CTA: the stream kernel from one row per SM (not with FP8)
-    assert frn.plan_launch(1000, 16384, 8, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
-    assert frn.plan_launch(1000, 16384, 8, 3, True, 152)["kernel"] == frn.KERNEL_STREAM
-    assert frn.plan_launch(1000, 16384, 8, 1, True, 152)["kernel"] == frn.KERNEL_ROWS
+    # rows wider than one CTA at many rows: one CTA a row, two tiles a warp, with R <= 8
+    for quant in (0, 1, 3):
+        pl = frn.plan_launch(1000, 16384, 8, quant, True, 152)
+        assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, quant
+    # R > 8: two tiles a warp with an FP8 output, or up to 22 tiles; else the stream kernel
     assert frn.plan_launch(1000, 8192, 16, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
-    # ... except with R <= 4 at many rows: one CTA a row, two tiles a warp
+    assert frn.plan_launch(1000, 16384, 12, 4, True, 152)["kernel"] == frn.KERNEL_STREAM
+    assert frn.plan_launch(1000, 6144, 9, 3, True, 152)["kernel"] == frn.KERNEL_STREAM
+    for R, H, quant in ((16, 8192, 1), (12, 16384, 2), (9, 5120, 0), (16, 5632, 4), (10, 4104, 3)):
+        pl = frn.plan_launch(1000, H, R, quant, True, 152)
+        assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, (R, H, quant)
+    assert frn.plan_launch(75, 16384, 16, 1, True, 152)["ctas_per_row"] == 4        # few rows: clusters
+    assert frn.plan_launch(75, 5120, 16, 0, True, 152)["kernel"] == frn.KERNEL_ROWS
     for quant in (0, 1, 2, 4):
         pl = frn.plan_launch(8192, 16384, 2, quant, True, 152)
         assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2 and pl["threads"] == 1024
     assert frn.plan_launch(8192, 16384, 2, 3, True, 152)["kernel"] == frn.KERNEL_STREAM   # MXFP4 without y
     for R, quant in ((3, 0), (4, 1), (4, 3), (4, 4)):
         assert frn.plan_launch(4096, 16384, R, quant, True, 152)["tiles_per_warp"] == 2, (R, quant)
-    assert frn.plan_launch(4096, 16384, 5, 0, True, 152)["kernel"] == frn.KERNEL_STREAM
-    for R in (5, 8):   # R = 5..8 in two stages, with an FP8 output only
-        assert frn.plan_launch(2048, 16384, R, 2, True, 152)["tiles_per_warp"] == 2
-        assert frn.plan_launch(2048, 16384, R, 4, True, 152)["kernel"] == frn.KERNEL_STREAM
+    for R in (5, 8):   # R = 5..8 in stages of four, every output
+        for quant in (0, 2, 4):
+            assert frn.plan_launch(2048, 16384, R, quant, True, 152)["tiles_per_warp"] == 2, (R, quant)
     assert frn.plan_launch(8192, 10000, 1, 0, True, 152)["threads"] == 20 * 32    # 40 tiles, ragged
     assert frn.plan_launch(75, 16384, 2, 0, True, 152)["tiles_per_warp"] == 1     # few rows: clusters
     assert frn.plan_launch(76, 16384, 4, 1, True, 152)["tiles_per_warp"] == 2

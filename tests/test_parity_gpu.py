@@ -198,7 +198,7 @@ def test_many_row_launches_are_bit_identical(R):
     (2, 5000, 256, True),     # packed short rows, eight to a CTA
     (2, 700, 7168, False),    # no residual: R loads a row
     (8, 1171, 7168, False),
-    (12, 400, 16384, True),   # cluster rows, R > 8, from two waves on (FP8 output)
+    (12, 400, 16384, True),   # two tiles a warp, R > 8 in stages of four (FP8 output)
     (8, 400, 16384, True),    # two tiles a warp, partials in two stages (FP8 output)
 ])
 def test_prefetch_ahead_paths(R, T, H, with_residual):
@@ -228,12 +228,15 @@ def test_prefetch_ahead_paths(R, T, H, with_residual):
     (1, 500, 16384, False), (2, 304, 8448, True), (4, 330, 16384, True), (3, 400, 12288, True),
     (4, 310, 9000, False), (8, 330, 16384, True), (6, 300, 12288, True), (5, 200, 8448, True),
     (3, 200, 7168, True), (4, 400, 8192, False), (4, 333, 6656, True), (3, 160, 7800, True),
-    (2, 2500, 7168, True),
+    (2, 2500, 7168, True), (7, 300, 16384, False), (5, 250, 12288, True), (16, 200, 5120, True),
+    (12, 160, 12288, True), (10, 180, 5000, True), (16, 100, 5120, False), (9, 90, 16384, True),
+    (12, 700, 5120, True),
 ])
 def test_two_tiles_per_warp(R, T, H, with_residual):
-    """Rows of 33..64 tiles with R <= 4 at many rows (and of 26..32 tiles with
-    R = 3 or 4 beyond one row per SM, or R = 2 with FP8 A from 16 rows an SM)
-    take one CTA per row, two tiles a warp: every row against the oracle, and
+    """Rows of 33..64 tiles with R <= 8 at many rows (and of 26..32 tiles with
+    R = 3 or 4 beyond one row per SM, or R = 2 with FP8 A from 16 rows an SM;
+    and of 17..64 tiles with R > 8 and an FP8 output, or up to 22 tiles) take
+    one CTA per row, two tiles a warp: every row against the oracle, and
     the bits of the cluster and stream kernels (and, past 32 tiles, of a
     forced launch at decode size, prefetch on; at 26..32 tiles T <= 2 waves
     prefetches before the wait by itself)."""
@@ -464,6 +467,33 @@ def test_stream_consumer_groups(groups, R, T, H):
         frn.set_kernel(frn.KERNEL_AUTO)
 
 
+def test_cluster_rows_prefetch_ahead_forced():
+    """Cluster rows from two waves on prefetch the rows a fixed distance ahead.
+    The planner gives such rows two tiles a warp instead, so clusters of 4 are
+    forced: R = 12, T = 400, H = 16384 with an FP8 output against the oracle,
+    and the same bits with every prefetch off and on the planner's choice."""
+    R, T, H = 12, 400, 16384
+    inp = syn.make_inputs(R, T, H, seed=95, partial_std=0.5)
+    d = DevInputs(inp)
+    auto = gpu_quant(d, True)
+    frn.set_kernel(frn.KERNEL_ROWS)
+    frn.set_ctas_per_row(4)
+    try:
+        assert frn.query_launch(T, H, R, 2)[1] == 4
+        check_quant(inp, f"forced clusters R={R} T={T} H={H}")
+        clusters = gpu_quant(d, True)
+        frn.set_l2_prefetch(1)
+        off = gpu_quant(d, True)
+    finally:
+        frn.set_l2_prefetch(0)
+        frn.set_ctas_per_row(0)
+        frn.set_kernel(frn.KERNEL_AUTO)
+    for a, b, c in zip(auto, clusters, off):
+        if a is not None:
+            assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+            assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(c).view(np.uint8))
+
+
 @pytest.mark.parametrize("R,T,H", [(16, 600, 4096), (9, 500, 2048), (10, 1000, 4096), (16, 457, 3968),
                                    (12, 460, 1024)])
 def test_staged_loads(R, T, H):
@@ -489,12 +519,11 @@ def test_staged_loads(R, T, H):
                 assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
 
 
-@pytest.mark.parametrize("R,T,H", [(2, 60, 16384), (8, 60, 12288), (1, 70, 8320), (12, 400, 16384)])
+@pytest.mark.parametrize("R,T,H", [(2, 60, 16384), (8, 60, 12288), (1, 70, 8320), (12, 70, 16384)])
 def test_wide_fp8_rows_on_clusters(R, T, H):
-    """FP8 output on rows wider than 8192 below half a wave, or with R > 8: the
-    planner takes the row kernel's clusters (with the prefetch ahead from two
-    waves on); every row against the oracle, and the same bits as the stream
-    kernel."""
+    """FP8 output on rows wider than 8192 below half a wave: the planner takes
+    the row kernel's clusters; every row against the oracle, and the same bits
+    as the stream kernel."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = frn.plan_launch(T, H, R, 1, True, sms)
     assert plan["kernel"] == frn.KERNEL_ROWS and plan["ctas_per_row"] > 1, plan
