@@ -709,6 +709,7 @@ PROFILE_CASES = {
     "staged_R16_T600_H4096": (16, 600, 4096, "norm", False, 0.5),
     "stream_R16_T862_H8192": (16, 862, 8192, "norm", False, 0.5),
     "row2_R16_T1379_H5120": (16, 1379, 5120, "norm", False, 0.5),
+    "row2_R10_T2520_H4096_quant_b": (10, 2520, 4096, "quant_b", False, 0.5),
     "R2_T2048_H16384_quant_a": (2, 2048, 16384, "quant_a", True, 1.0),
     "R4_T2048_H16384_quant_b": (4, 2048, 16384, "quant_b", False, 0.5),
     "R8_T1024_H16384_quant_a": (8, 1024, 16384, "quant_a", False, 0.5),

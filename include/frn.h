@@ -329,7 +329,7 @@ frn_status frn_set_stream_groups(int groups);
  *   tiles_per_cta   row kernel: warps (32-vector tiles) a row has in a CTA
  *   tiles_per_warp  stream kernel: tiles a consumer warp holds; row kernel: 2
  *                   when one CTA holds a row at two tiles a warp (rows of
- *                   26..64 tiles), else 1
+ *                   9..64 tiles), else 1
  *   threads, grid   threads per CTA, CTAs in the grid
  *   groups, consumer_warps, slots, smem_bytes
  *                   stream kernel: consumer groups, warps a group, ring slots

@@ -144,6 +144,17 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // on clusters of 4; R = 12, H = 12288 FP8 B 50.7 / 63.9 us), the stream
 // kernel otherwise (no quant 48.9 / 46.1 us).
 //
+// Rows of 9..16 tiles with R > 8 against the staged one-tile-a-warp CTA
+// (two-tile / staged or single CTA, us): better up to R = 10 at every output
+// (H = 4096, R = 10, T = 2520 no quant 44.2 / 44.5, FP8 B 46.3 / 51.3, MXFP4
+// B 45.3 / 48.4, T = 315 8.0 / 9.1; R = 9, T = 2730 FP8 A 43.5 / 47.6;
+// H = 2304, R = 10, T = 560 FP8 B 8.0 / 9.5), and with R = 11, 12 for a quant
+// output at staged sizes (H = 3072, R = 11, T = 3120 FP8 B 46.4 / 51.9; R =
+// 12, T = 2912 46.5 / 48.9), but not without one (R = 12 no quant 44.5 /
+// 43.3), below three waves (H = 4096, R = 11, T = 292 FP8 B 8.5 / 8.0), or
+// from R = 13 on (R = 16, T = 1724 no quant 47.6 / 42.1: the staged CTA has
+// twice the warps for the same bytes in flight).
+//
 // Rows of 26..32 tiles (6144 < H <= 8192) with R = 3 or 4 beyond one row per
 // SM: the wide CTA (832..1024 threads at 40 registers) leaves room for one
 // row an SM, two-tile CTAs of half as many threads for two, so twice the
@@ -160,7 +171,10 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // quant, FP8 B and MXFP4 level; T = 586 8.63 / 8.50).
 bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
     const bool fp8 = quant == 1 || quant == 2;
-    if (ntiles <= frn::kMaxTilesPerCta) return false;
+    if (ntiles <= frn::kMaxTilesPerCta) {
+        if (ntiles <= 8 || R <= 8 || 2 * T < num_sms) return false;
+        return R <= 10 || (R <= 12 && quant != 0 && T >= 3LL * num_sms);
+    }
     if (R > 8) return (fp8 || ntiles <= 22) && 2 * T >= num_sms;
     if (ntiles > 2 * frn::kMaxTilesPerCta) return !(quant == 3 && R <= 2) && 2 * T >= num_sms;
     if (ntiles >= 26)
@@ -257,7 +271,8 @@ bool staged_window(long long T, int H, int R, int num_sms) {
 
 frn::RowPlan plan_rows(long long T, int H, int R, int quant, int num_sms) {
     frn::RowPlan plan = choose_rows(T, H, R, quant, num_sms);
-    if (plan.ctas_per_row == 1 && plan.rows_per_cta == 1 && staged_window(T, H, R, num_sms))
+    if (plan.tiles_per_warp == 1 && plan.ctas_per_row == 1 && plan.rows_per_cta == 1 &&
+        staged_window(T, H, R, num_sms))
         plan.staged = 1;
     return plan;
 }

@@ -4,8 +4,8 @@
 //                   cluster, or several short rows per CTA; all of a thread's
 //                   loads in flight at once (in stages of two for R > 8); every
 //                   row that fits one CTA, at any T.  Its two-tiles-a-warp
-//                   variant holds a row of 26..64 tiles on one CTA at many
-//                   rows (R <= 4, or up to 8 with an FP8 output).
+//                   variant holds a row of 9..64 tiles on one CTA at many
+//                   rows (partials in stages of four for R > 4).
 //  * frn_stream.cuh stream kernel: persistent, TMA bulk copies into a shared-
 //                   memory ring, warp-specialised; for the other rows wider
 //                   than one CTA.

@@ -1,6 +1,6 @@
 // frn_rows.cuh -- the row kernel: one token row per CTA or per thread-block
 // cluster, or several short rows per CTA; and its two-tiles-a-warp variant
-// (frn_row2_kernel) for rows of 26..64 tiles on one CTA.
+// (frn_row2_kernel) for rows of 9..64 tiles on one CTA.
 //
 // The tiles of a row go to one CTA (up to 1024 threads) or are spread over C
 // CTAs of one cluster (tiles_per_cta warps each, one tile per warp): a row too
@@ -328,8 +328,10 @@ frn_row_kernel(const __grid_constant__ Params p) {
 // while a whole row's loads are in flight on one SM (with R > 4, in stages of
 // four partials, so that they fit 64 registers).  Rows of 26..32 tiles take it
 // too with R = 2..4 at many rows (at up to 512 threads two rows fit an SM,
-// where the one-tile-a-warp CTA leaves room for one), and rows of 17..32 tiles
-// with R > 8, which no one-tile-a-warp CTA holds in registers.  Same
+// where the one-tile-a-warp CTA leaves room for one), rows of 17..32 tiles
+// with R > 8, which no one-tile-a-warp CTA holds in registers, and rows of
+// 9..16 tiles with R = 9..12 (four partials in flight a stage instead of the
+// staged CTA's two).  Same
 // per-vector arithmetic, tile sums and tree as frn_row_kernel, so the same
 // bits.
 template <int RMAX, int MODE>
@@ -390,7 +392,10 @@ __global__ void __launch_bounds__(1024, 1) frn_row2_kernel(const __grid_constant
                     if (r < p.R) add8(accs[t], a[t][r]);
             }
         }
-#pragma unroll
+        // up to 16 partials the stages stay a loop: unrolled, they spilled 40
+        // bytes a thread and ran 1-8 % slower (R = 9, H = 5120, T = 2184:
+        // 48.0 vs 44.0 us)
+#pragma unroll (RMAX > 8 ? 1 : RMAX / 4)
         for (int s = 1; s < RMAX / 4; ++s) {
             if (4 * s >= p.R) break;
             uint4 b[2][4];
@@ -571,7 +576,7 @@ cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t strea
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
 template <int MODE>
 cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
-    // two tiles a warp: one CTA per row of 17..64 tiles (the host plans
+    // two tiles a warp: one CTA per row of 9..64 tiles (the host plans
     // nothing else; R > 4 loads its partials in stages of four)
     if (plan.tiles_per_warp == 2) {
         if (p.R <= 1) return launch_row2<1, MODE>(p, plan, stream, pdl);

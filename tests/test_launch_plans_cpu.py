@@ -29,6 +29,9 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
         assert pl["kernel"] == frn.KERNEL_ROWS, what                    # every row that fits one CTA
     if auto and ntiles > 32 and R <= 8 and 2 * T >= sms and not (quant == 3 and R <= 2):
         assert pl["kernel"] == frn.KERNEL_ROWS and pl["tiles_per_warp"] == 2, what
+    if auto and 8 < ntiles <= 16 and R > 8:                            # against the staged CTA
+        two = 2 * T >= sms and (R <= 10 or (R <= 12 and quant != 0 and T >= 3 * sms))
+        assert pl["tiles_per_warp"] == (2 if two else 1) and (not two or not pl["staged"]), what
     if auto and ntiles > 16 and R > 8:                                  # no one-tile-a-warp CTA holds the row
         two = (quant in (1, 2) or ntiles <= 22) and 2 * T >= sms
         if two:
@@ -44,7 +47,7 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
         assert C * tpc >= ntiles and (C - 1) * tpc < ntiles, what          # every tile, no empty CTA
         if pl["tiles_per_warp"] == 2:                                      # two tiles a warp, one CTA a row
             assert C == 1 and rows == 1 and tpc <= 64, what
-            assert tpc > 32 or (tpc >= 26 and 2 <= R <= 4) or (tpc > 16 and R > 8), what
+            assert tpc > 32 or (tpc >= 26 and 2 <= R <= 4) or (tpc > 8 and R > 8), what
             assert thr == -(-tpc // 2) * 32 and not pl["staged"], what
         else:
             assert pl["tiles_per_warp"] == 1 and thr == rows * tpc * 32 and thr <= 1024, what

@@ -230,7 +230,8 @@ def test_prefetch_ahead_paths(R, T, H, with_residual):
     (3, 200, 7168, True), (4, 400, 8192, False), (4, 333, 6656, True), (3, 160, 7800, True),
     (2, 2500, 7168, True), (7, 300, 16384, False), (5, 250, 12288, True), (16, 200, 5120, True),
     (12, 160, 12288, True), (10, 180, 5000, True), (16, 100, 5120, False), (9, 90, 16384, True),
-    (12, 700, 5120, True),
+    (12, 700, 5120, True), (10, 1000, 4096, True), (9, 100, 2312, True), (12, 500, 3072, True),
+    (11, 470, 4096, True),
 ])
 def test_two_tiles_per_warp(R, T, H, with_residual):
     """Rows of 33..64 tiles with R <= 8 at many rows (and of 26..32 tiles with
@@ -494,7 +495,7 @@ def test_cluster_rows_prefetch_ahead_forced():
             assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(c).view(np.uint8))
 
 
-@pytest.mark.parametrize("R,T,H", [(16, 600, 4096), (9, 500, 2048), (10, 1000, 4096), (16, 457, 3968),
+@pytest.mark.parametrize("R,T,H", [(16, 600, 4096), (9, 500, 2048), (14, 1000, 4096), (16, 457, 3968),
                                    (12, 460, 1024)])
 def test_staged_loads(R, T, H):
     """Rows whose partials are loaded in stages (two stages of two in flight),
