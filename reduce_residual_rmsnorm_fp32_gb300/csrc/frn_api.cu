@@ -168,7 +168,13 @@ bool wide_possible(int ntiles, int R) { return ntiles <= 2 * frn::kMaxTilesPerCt
 // T = 1171 17.65 / 17.32); within one row per SM the wide CTA's extra warps
 // win (H = 7168, R = 4, T = 64 2.44 / 2.35, T = 147 3.56 / 3.47).  With R = 2
 // only FP8 A at 16 rows an SM and more (T = 8192, H = 7168 79.9 / 81.3; no
-// quant, FP8 B and MXFP4 level; T = 586 8.63 / 8.50).
+// quant, FP8 B and MXFP4 level; T = 586 8.63 / 8.50).  With R = 5..8 from one
+// to 1.65 rows an SM, where the wide CTA runs a second, partial wave and the
+// two-tile grid fits one (H = 7168, R = 8, T = 180 6.32 / 7.25, FP8 B 7.17 /
+// 7.83, T = 230 7.12 / 7.71, T = 250 7.67 / 8.03; R = 5, T = 200 5.02 / 6.25;
+// R = 6, T = 250 FP8 A 6.55 / 7.33; R = 7, T = 200 6.07 / 7.13; H = 8192,
+// R = 8, T = 200 7.38 / 8.32), but not beyond (R = 8, T = 280 8.48 / 8.20,
+// T = 1171 31.3 / 30.2).
 bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
     const bool fp8 = quant == 1 || quant == 2;
     if (ntiles <= frn::kMaxTilesPerCta) {
@@ -178,7 +184,8 @@ bool two_tile_rows(long long T, int ntiles, int R, int quant, int num_sms) {
     if (R > 8) return (fp8 || ntiles <= 22) && 2 * T >= num_sms;
     if (ntiles > 2 * frn::kMaxTilesPerCta) return !(quant == 3 && R <= 2) && 2 * T >= num_sms;
     if (ntiles >= 26)
-        return ((R == 3 || R == 4) && T > num_sms) || (R == 2 && quant == 1 && T >= 16LL * num_sms);
+        return ((R == 3 || R == 4) && T > num_sms) || (R == 2 && quant == 1 && T >= 16LL * num_sms) ||
+               (R >= 5 && T > num_sms && 20 * T <= 33LL * num_sms);
     return false;
 }
 

@@ -39,7 +39,8 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
         else:
             assert pl["kernel"] == frn.KERNEL_STREAM or pl["tiles_per_warp"] == 1, what
     if auto and 17 <= ntiles <= 32 and R <= 8:                          # rows a wide CTA could hold
-        two = ntiles >= 26 and ((R in (3, 4) and T > sms) or (R == 2 and quant == 1 and T >= 16 * sms))
+        two = ntiles >= 26 and ((R in (3, 4) and T > sms) or (R == 2 and quant == 1 and T >= 16 * sms) or
+                                (R >= 5 and sms < T and 20 * T <= 33 * sms))
         assert pl["tiles_per_warp"] == (2 if two else 1), what
     if pl["kernel"] == frn.KERNEL_ROWS:
         C, tpc, rows, thr = pl["ctas_per_row"], pl["tiles_per_cta"], pl["rows_per_cta"], pl["threads"]
@@ -157,9 +158,10 @@ def test_staged_plans():
     assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 1 and pl["threads"] == 512
     assert frn.plan_launch(300, 4096, 16, 0, True, 152)["staged"] == 0
     for quant in (0, 1, 2, 3, 4):
-        for R, T in ((8, 586), (8, 1000), (5, 586), (4, 1519), (8, 1063), (8, 4682), (3, 1171), (4, 152)):
+        for R, T in ((8, 586), (8, 1000), (5, 586), (4, 1519), (8, 1063), (8, 4682), (3, 1171), (4, 152),
+                     (8, 200), (6, 250), (8, 251), (7, 152)):
             pl = frn.plan_launch(T, 7168, R, quant, True, 152)
-            two = R <= 4 and T > 152
+            two = T > 152 and (R <= 4 or T <= 250)
             assert pl["kernel"] == frn.KERNEL_ROWS and pl["staged"] == 0, (R, T, quant)
             assert pl["threads"] == (448 if two else 896) and pl["tiles_per_warp"] == (2 if two else 1), (R, T, quant)
         # R = 2: two tiles a warp only with an FP8 output without y from 16 rows an SM
