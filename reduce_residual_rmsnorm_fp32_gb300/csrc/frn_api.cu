@@ -532,8 +532,10 @@ frn::Params make_params(const Call& c, const frn::RowPlan& rplan, const frn::Str
 // (32) and the registers the kernel's launch bound holds (row_min_blocks).
 long long row_ctas_per_sm(const frn::RowPlan& plan, int R) {
     if (plan.tiles_per_warp == 2) {
-        // frn_row2_kernel: launch bound (1024, 1), so up to 64 registers a thread
-        const long long by_threads = 2048 / plan.threads, by_regs = 65536 / (plan.threads * 64LL);
+        // frn_row2_kernel: launch bound (1024, 1), so up to 64 registers a
+        // thread; (640, 2), 48 registers, for R <= 2 at 608..640 threads
+        const long long regs = R <= 2 && plan.threads > 576 && plan.threads <= 640 ? 48 : 64;
+        const long long by_threads = 2048 / plan.threads, by_regs = 65536 / (plan.threads * regs);
         return by_threads < by_regs ? by_threads : by_regs;
     }
     const bool cluster = plan.ctas_per_row > 1;

@@ -333,9 +333,10 @@ frn_row_kernel(const __grid_constant__ Params p) {
 // 9..16 tiles with R = 9..12 (four partials in flight a stage instead of the
 // staged CTA's two).  Same
 // per-vector arithmetic, tile sums and tree as frn_row_kernel, so the same
-// bits.
-template <int RMAX, int MODE>
-__global__ void __launch_bounds__(1024, 1) frn_row2_kernel(const __grid_constant__ Params p) {
+// bits.  MINB = 2 (at most 640 threads, 48 registers) fits two such CTAs of
+// 608..640 threads on an SM, where the default bound's 52 registers fit one.
+template <int RMAX, int MODE, int MINB = 1>
+__global__ void __launch_bounds__(MINB == 1 ? 1024 : 640, MINB) frn_row2_kernel(const __grid_constant__ Params p) {
     __shared__ float tile_sum[kMaxTiles];
     __shared__ float rstd_sh;
     const int warp = threadIdx.x >> 5;
@@ -558,7 +559,7 @@ cudaError_t launch_row_one(const Params& p, const RowPlan& plan, cudaStream_t st
     return cudaLaunchKernelEx(&cfg, frn_row_kernel<RMAX, MODE, CLUSTER, MAXT, STAGED>, p);
 }
 
-template <int RMAX, int MODE>
+template <int RMAX, int MODE, int MINB = 1>
 cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t stream, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
@@ -570,7 +571,7 @@ cudaError_t launch_row2(const Params& p, const RowPlan& plan, cudaStream_t strea
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, frn_row2_kernel<RMAX, MODE>, p);
+    return cudaLaunchKernelEx(&cfg, frn_row2_kernel<RMAX, MODE, MINB>, p);
 }
 
 // Dispatch on the unrolled partial count and on whether the row spans a cluster.
@@ -579,6 +580,14 @@ cudaError_t launch_rows(const Params& p, const RowPlan& plan, cudaStream_t strea
     // two tiles a warp: one CTA per row of 9..64 tiles (the host plans
     // nothing else; R > 4 loads its partials in stages of four)
     if (plan.tiles_per_warp == 2) {
+        // R <= 2 rows of 37..40 tiles: two CTAs an SM at 48 registers (H = 10240,
+        // T = 3276, R = 1 FP8 A 52.3 -> 39.2 us, FP8 B 57.2 -> 48.7 us; R = 2
+        // FP8 A 47.0 -> 38.5 us, MXFP4 B 47.4 -> 44.2 us, no quant 42.6 ->
+        // 41.9 us); with R > 2 the loads need more registers
+        if (p.R <= 2 && plan.threads > 576 && plan.threads <= 640) {
+            if (p.R <= 1) return launch_row2<1, MODE, 2>(p, plan, stream, pdl);
+            return launch_row2<2, MODE, 2>(p, plan, stream, pdl);
+        }
         if (p.R <= 1) return launch_row2<1, MODE>(p, plan, stream, pdl);
         if (p.R <= 2) return launch_row2<2, MODE>(p, plan, stream, pdl);
         if (p.R <= 4) return launch_row2<4, MODE>(p, plan, stream, pdl);

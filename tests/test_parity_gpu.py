@@ -231,7 +231,8 @@ def test_prefetch_ahead_paths(R, T, H, with_residual):
     (2, 2500, 7168, True), (7, 300, 16384, False), (5, 250, 12288, True), (16, 200, 5120, True),
     (12, 160, 12288, True), (10, 180, 5000, True), (16, 100, 5120, False), (9, 90, 16384, True),
     (12, 700, 5120, True), (10, 1000, 4096, True), (9, 100, 2312, True), (12, 500, 3072, True),
-    (11, 470, 4096, True), (8, 200, 7168, True), (6, 240, 8192, False),
+    (11, 470, 4096, True), (8, 200, 7168, True), (6, 240, 8192, False), (1, 400, 10240, True),
+    (2, 330, 9728, False),
 ])
 def test_two_tiles_per_warp(R, T, H, with_residual):
     """Rows of 33..64 tiles with R <= 8 at many rows (and of 26..32 tiles with
