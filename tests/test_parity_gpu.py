@@ -199,7 +199,7 @@ def test_many_row_launches_are_bit_identical(R):
     (2, 700, 7168, False),    # no residual: R loads a row
     (8, 1171, 7168, False),
     (12, 400, 16384, True),   # two tiles a warp, R > 8 in stages of four (FP8 output)
-    (8, 400, 16384, True),    # two tiles a warp, partials in two stages (FP8 output)
+    (8, 400, 16384, True),    # two tiles a warp, partials in stages of four (FP8 output)
 ])
 def test_prefetch_ahead_paths(R, T, H, with_residual):
     """Grids of more than one wave, where each CTA prefetches the rows a fixed
