@@ -288,8 +288,9 @@ int frn_version(void);
  *   stream; the kernel still waits for that kernel's completion before its
  *   first global-memory load or store (only an L2 prefetch hint, which hands
  *   no value to the kernel, may precede the wait).  0 launches plainly.
- * frn_set_kernel: 0 (default) picks the kernel from T, H and the SM count;
- *   1 forces the row kernel (a row per CTA, wide CTA or thread-block cluster,
+ * frn_set_kernel: 0 (default) picks the kernel from T, H, R, the output and
+ *   the SM count; 1 forces the row kernel (a row per CTA -- one tile a warp,
+ *   or two for rows of 9..64 tiles -- per wide CTA or thread-block cluster,
  *   or several short rows per CTA; registers hold each row),
  *   2 forces the stream kernel (persistent, one CTA per SM, rows streamed
  *   through shared memory with TMA bulk copies, for many rows).
@@ -297,7 +298,8 @@ int frn_version(void);
  *   and the SM count between one CTA per row (several short rows per CTA when
  *   H <= 1024 and T is large) and a cluster of CTAs per row;
  *   1 forces one CTA per row (up to 1024 threads when H <= 8192 and R <= 8,
- *   else the smallest cluster that holds the row); 2..16 force a cluster of
+ *   two tiles a warp when H > 8192, else the smallest cluster that holds the
+ *   row); 2..16 force a cluster of
  *   that many CTAs (rounded so that no CTA is empty; 9..16 is a non-portable
  *   cluster size, with at least two tiles a CTA).
  * frn_set_stream_groups: stream kernel only.  0 (default) chooses how many
