@@ -13,7 +13,7 @@ import reduce_residual_rmsnorm_fp32_gb300 as frn
 from reduce_residual_rmsnorm_fp32_gb300 import _build
 
 SMEM_LIMIT = 232448
-TS = (1, 3, 8, 16, 33, 64, 127, 300, 608, 1171, 8192, 65536)
+TS = (1, 3, 8, 16, 33, 64, 127, 200, 300, 608, 1171, 2500, 8192, 65536)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,7 +48,7 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
         assert C * tpc >= ntiles and (C - 1) * tpc < ntiles, what          # every tile, no empty CTA
         if pl["tiles_per_warp"] == 2:                                      # two tiles a warp, one CTA a row
             assert C == 1 and rows == 1 and tpc <= 64, what
-            assert tpc > 32 or (tpc >= 26 and 2 <= R <= 4) or (tpc > 8 and R > 8), what
+            assert tpc > 32 or (tpc >= 26 and 2 <= R <= 8) or (tpc > 8 and R > 8), what
             assert thr == -(-tpc // 2) * 32 and not pl["staged"], what
         else:
             assert pl["tiles_per_warp"] == 1 and thr == rows * tpc * 32 and thr <= 1024, what
@@ -78,7 +78,7 @@ def _check_plan(pl, T, H, R, quant, residual, sms, auto=True):
 def test_every_hidden_size_plans_a_valid_launch():
     n = 0
     for H in range(8, 16385, 8):
-        for R, T in itertools.product((1, 2, 3, 4, 8, 16), TS):
+        for R, T in itertools.product((1, 2, 3, 4, 5, 6, 8, 10, 12, 16), TS):
             quants = [0] + ([1, 2] if H % 128 == 0 else []) + ([3, 4] if H % 32 == 0 else [])
             for quant in quants:
                 for residual in (True, False):
@@ -92,7 +92,7 @@ def test_every_hidden_size_plans_a_valid_launch():
 
 @pytest.mark.parametrize("sms", [1, 8, 132, 148])
 def test_other_sm_counts(sms):
-    for H, R, T in itertools.product(range(256, 16385, 1280), (1, 2, 8, 16), TS):
+    for H, R, T in itertools.product(range(256, 16385, 1280), (1, 2, 4, 5, 8, 10, 16), TS):
         for residual in (True, False):
             _check_plan(frn.plan_launch(T, H, R, 0, residual, sms), T, H, R, 0, residual, sms)
 
